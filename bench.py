@@ -1,0 +1,358 @@
+"""Benchmark of the MoE FFN layer forward on GB300.
+
+Workload: the Qwen3-235B-shaped layer (H=4096, 128 experts, top-8 softmax
+renormalised, expert intermediate 1536, SwiGLU, no shared expert, bf16
+weights and activations), T = 8192 tokens (prefill), seeded synthetic inputs
+(x ~ N(0,1), router bias from Zipf(1.1) ranks, weights ~ N(0, 0.02)).
+
+One step = one moe_forward over the whole batch: route, permute, grouped
+GEMM gate/up + SwiGLU, grouped GEMM down, combine.  Inputs are resident in
+HBM; L2 is flushed (a 256 MB write) before every timed step, outside the
+step's events.  Each step records CUDA events at the stage boundaries
+(moe_forward_profiled), which gives the grouped-GEMM kernel time live.
+
+Prints one JSON line.  --impl reference times the fp64 CPU oracle on the
+same workload (bounded token samples per step) instead.
+
+Multi-GPU: the layer forward does not shard in this build (one GPU per
+process); under torchrun each rank runs an independent replica on its own
+GPU and the job value is the sum of tokens over the max per-rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+CFG = synth.QWEN3_235B
+T_MAIN = 8192
+T_DECODE = 256
+METRIC = "MoE-layer tokens/s (Qwen3-235B-shaped bf16 layer, T=8192)"
+UNIT = "tokens/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_tokens_per_s(cfg, acts, w_host, tokens):
+    """Time the fp64 oracle (as it stands) on `tokens` of the workload."""
+    import oracle
+    w13, w2 = w_host
+
+    def get_expert(e):
+        return oracle.ExpertWeights(w13[e].double().numpy(), w2[e].double().numpy())
+
+    x = acts.x.double().numpy()
+    t0 = time.perf_counter()
+    oracle.forward(x, acts.logits.numpy(), cfg.k, cfg.E, get_expert, None, tokens=tokens)
+    dt = time.perf_counter() - t0
+    return len(tokens) / dt, dt
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on the same workload, K timed steps of
+    bounded token samples."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    cfg, T = CFG, T_MAIN
+    acts = synth.make_activations(cfg, T, seed=0)
+    w = synth.make_weights(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    w_host = (w.w13.cpu(), w.w2.cpu())
+    del w
+    # size the per-step sample so that warmup + steps take about 3 minutes
+    probe = synth.sample_tokens(T, 8, seed=1)
+    _, t8 = oracle_tokens_per_s(cfg, acts, w_host, probe)
+    budget = 180.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(512, 8 * budget / max(t8, 1e-3))))
+    rates, times = [], []
+    for i in range(args.warmup + args.steps):
+        toks = synth.sample_tokens(T, n, seed=100 + i)
+        r, dt = oracle_tokens_per_s(cfg, acts, w_host, toks)
+        if i >= args.warmup:
+            rates.append(r)
+            times.append(dt)
+    total_tok = n * args.steps
+    value = total_tok / sum(times)
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"qwen3-235b moe layer bf16 weights, T={T} (oracle on {n}-token samples)",
+                   "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "T": T, "zipf": cfg.zipf},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} seeded tokens of the T={T} batch per step (rows are token-independent)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    from mixture_experts_layer_fwd_gb300 import MoELayer, api, moe_sync_status
+    from mixture_experts_layer_fwd_gb300 import build as _build
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    cfg, T = CFG, T_MAIN
+    acts = synth.make_activations(cfg, T, seed=0)
+    w = synth.make_weights(cfg, seed=0, device=str(dev))
+    layer = MoELayer.from_config(cfg, w)
+    x = acts.x.to(dev)
+    logits = acts.logits.to(dev)
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+    ws = layer.workspace(T)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs):
+        api.moe_forward_profiled(layer.c, x, logits, out, ws, evs)
+
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    warm = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    for ev in warm:
+        ev.record()  # creates the underlying CUDA events
+    for evs in evsets:
+        for ev in evs:
+            ev.record()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(warm)
+    torch.cuda.synchronize()
+    if moe_sync_status() != 0:
+        raise RuntimeError("device status not clean after warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evsets[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    if moe_sync_status() != 0:
+        raise RuntimeError("device status not clean after the timed steps")
+
+    step_ms = [evs[0].elapsed_time(evs[6]) for evs in evsets]
+    stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(6)] for evs in evsets])
+    total_ms = max_over_ranks(float(sum(step_ms)), world, dev)
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # grouped GEMM kernel: two launches per step (gate/up + SwiGLU, down)
+    flops = cfg.flops_per_token() * T
+    gemm_ms = float(np.mean(stage_ms[:, 3] + stage_ms[:, 4]))
+    p, src = peaks()
+    peak = p.get("bf16_tflops_sustained", p["bf16_tflops"])
+    achieved = flops / (gemm_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "grouped_gemm_kernel (2 launches/step)",
+                "peak_source": f"bf16_tflops_sustained of {src} peaks"}
+
+    # e2e through the C ABI with host buffers (pinned), copies inside the timing
+    xh = acts.x.pin_memory()
+    lh = acts.logits.pin_memory()
+    oh = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    ld = torch.empty_like(logits)
+    for _ in range(2):
+        api.moe_forward_host(layer.c, xh, lh, oh, xd, ld, out, ws)
+    e2e_t = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        api.moe_forward_host(layer.c, xh, lh, oh, xd, ld, out, ws)
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_s = max_over_ranks(float(np.mean(e2e_t)), world, dev)
+    h2d = T * cfg.H * 2 + T * cfg.E * 4
+    d2h = T * cfg.H * 2
+
+    # decode-size point on the same weights (weight-streaming bound)
+    Td = T_DECODE
+    xd_ = x[:Td].contiguous()
+    ld_ = logits[:Td].contiguous()
+    od_ = out[:Td]
+    dec = []
+    evd = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    for ev in evd:
+        ev.record()
+    for i in range(args.warmup + 10):
+        flush.zero_()
+        api.moe_forward_profiled(layer.c, xd_, ld_, od_, ws, evd)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            dec.append(evd[0].elapsed_time(evd[6]))
+    idx_d, _ = api.moe_route(ld_, cfg.k)
+    counts = torch.bincount(idx_d.reshape(-1).long(), minlength=cfg.E)
+    active = int((counts > 0).sum())
+    wbytes = active * 3 * cfg.H * cfg.I * 2
+    dec_ms = float(np.median(dec))
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"qwen3-235b moe layer bf16, T={T}", "H": cfg.H, "E": cfg.E, "k": cfg.k,
+                   "I": cfg.I, "T": T, "zipf": cfg.zipf, "seed": 0,
+                   "l2": "flushed before every step (256 MB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "stage_ms": {n: round(float(np.mean(stage_ms[:, i])), 4) for i, n in
+                     enumerate(["route", "quant", "permute", "gemm_gate_up", "gemm_down", "combine"])},
+        "e2e": {"value": round(world * T / e2e_s, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 8 * args.steps,
+        "clocks": clocks,
+        "decode_T256": {"ms": round(dec_ms, 4), "tokens_per_s": round(Td / (dec_ms / 1e3), 1),
+                        "active_experts": active,
+                        "weight_gbs": round(wbytes / (dec_ms / 1e3) / 1e9, 1),
+                        "hbm_frac": round(wbytes / (dec_ms / 1e3) / 1e9 / p["hbm_gbs"], 4)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w_host = (w.w13.cpu(), w.w2.cpu())
+        toks = synth.sample_tokens(T, args.cpu_tokens, seed=1)
+        r, dt = oracle_tokens_per_s(cfg, acts, w_host, toks)
+        line["cpu_baseline"] = {"value": round(r, 3), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"{len(toks)} seeded tokens of the T={T} batch "
+                                          f"({dt:.1f} s of fp64 CPU work; rows are token-independent)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

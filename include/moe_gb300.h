@@ -1,0 +1,273 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) top-k routed MoE FFN layer
+ * forward.
+ *
+ * The layer computes, for every token t,
+ *
+ *     out_t = sum_{j<k} w[t,j] * E_{idx[t,j]}(x_t) + S(x_t)
+ *
+ * where E_e is a SwiGLU expert (gate/up projection, silu(gate) * up, down
+ * projection) and S an always-on shared expert ("Hosting Qwen on Blackwell",
+ * sections "MoE Dispatch - Combine" and "MoE GEMM"; "Como Servimos um Modelo
+ * MoE de 397B com 4.7x de Speedup em TPU v7", MoE FFN description; "CuTeDSL
+ * at Perplexity", local dispatch / combine kernels).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every call returns an int status (MOE_OK or one of MOE_ERR_*).
+ *  - All tensors are caller-owned DEVICE pointers unless a parameter says
+ *    "host".  The library never allocates or frees memory: scratch space is a
+ *    caller-supplied workspace whose size the matching *_workspace_size()
+ *    call returns.  Workspaces must be 256-byte aligned.
+ *  - Every call is asynchronous on the caller's CUDA stream (`stream` is a
+ *    cudaStream_t passed as void*; NULL is the legacy default stream).  The
+ *    library does no host synchronisation except in moe_sync_status() and
+ *    moe_forward_host().
+ *  - Layouts are row-major with the innermost dimension contiguous.  bf16
+ *    tensors are passed as uint16_t bit patterns.
+ *  - NVFP4 tensors are three arrays: packed E2M1 codes (uint8, element 2j in
+ *    the low nibble, 2j+1 in the high nibble), one E4M3 scale byte per 16
+ *    consecutive elements along the reduction dimension (row-major
+ *    [rows, cols/16]), and an fp32 global scale.  Decoded value =
+ *    e2m1(q) * e4m3(s) * g ("Driving vLLM WideEP and Large-Scale Serving
+ *    Toward Maturity on Blackwell (Part I)", sections "NVFP4 GEMM for MoE and
+ *    O-proj" and "NVFP4 MoE dispatch").
+ *  - Argument errors are detected on the host before anything is launched:
+ *    MOE_ERR_INVALID_ARG (null or misaligned pointer, negative size),
+ *    MOE_ERR_UNSUPPORTED (shape outside what the kernels handle, see each
+ *    call), MOE_ERR_WORKSPACE (workspace too small).  Launch failures return
+ *    MOE_ERR_CUDA; moe_last_cuda_error() gives the CUDA message.
+ *  - The only device-side waits are mbarrier waits inside one thread block.
+ *    Each is bounded in time (moe_set_wait_timeout_ns, default 1 s); a wait
+ *    that runs out records MOE_ERR_TIMEOUT in a device error word and the
+ *    kernel returns.  moe_sync_status() reports (and clears) it.
+ *  - Inputs are assumed finite; NaN / Inf inputs give unspecified results.
+ *  - T = 0 (no tokens) is a valid no-op returning MOE_OK.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1
+#define MOE_ERR_UNSUPPORTED 2
+#define MOE_ERR_WORKSPACE 3
+#define MOE_ERR_CUDA 4
+#define MOE_ERR_TIMEOUT 5
+
+/* ------------------------------------------------------------ data formats */
+#define MOE_FMT_BF16 0
+#define MOE_FMT_NVFP4 1
+
+/* -------------------------------------------------- grouped GEMM epilogues */
+#define MOE_EPI_STORE_BF16 0   /* C = A * W^T, rounded to bf16                        */
+#define MOE_EPI_SWIGLU_BF16 1  /* W has 2N rows per group: gate [0,N), up [N,2N);
+                                  C = silu(A W_gate^T) * (A W_up^T), rounded to bf16   */
+#define MOE_EPI_SWIGLU_NVFP4 2 /* as SWIGLU_BF16, but the fp32 result is quantised to
+                                  NVFP4 with a caller-given global scale              */
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int moe_version(void);
+
+/* Static string for a status code. */
+const char* moe_status_string(int status);
+
+/* Message of the last CUDA error seen by this library in this process
+ * (thread-unsafe, diagnostic only). */
+const char* moe_last_cuda_error(void);
+
+/* Time limit of every device-side wait, in nanoseconds (default 1e9).
+ * ns == 0 restores the default. */
+int moe_set_wait_timeout_ns(unsigned long long ns);
+
+/* Synchronises `stream`, then returns MOE_ERR_TIMEOUT if any kernel of this
+ * library recorded a wait time-out since the last call (clearing the record),
+ * MOE_ERR_CUDA on a CUDA error, else MOE_OK. */
+int moe_sync_status(void* stream);
+
+/* Test hook for the time-out path: launches one block whose thread waits on
+ * an mbarrier that nothing ever arrives on, with the library's bounded wait.
+ * The wait gives up after `timeout_ns`, records MOE_ERR_TIMEOUT in the device
+ * error word and the kernel returns; the context stays usable.  Read the
+ * result with moe_sync_status(). */
+int moe_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/* ------------------------------------------------------------------- route
+ * Router softmax and top-k with renormalised weights.
+ * Pages: the routing table holds expert indices and weights of shape [T, k]
+ * ("Como Servimos um Modelo MoE de 397B ...", section "Tres coletivas viram
+ * duas"); the softmax / top-k / renormalisation is the layer's stated router.
+ *
+ *   logits : fp32 [T, E]   router logits (x W_r + bias, computed upstream)
+ *   idx    : int32 [T, k]  chosen experts, by descending logit; equal logits
+ *                          are ordered by ascending expert id
+ *   w      : fp32 [T, k]   w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the
+ *                          k chosen logits (= softmax over E renormalised)
+ * One warp per token.  Supports 1 <= k <= min(E, 32), 1 <= E <= 1024. */
+int moe_route(const float* logits, int T, int E, int k,
+              int32_t* idx, float* w, void* stream);
+
+/* ----------------------------------------------------------------- permute
+ * Local dispatch: count tokens per expert, give each routed slot a unique
+ * position inside its expert's list, copy the token rows into an
+ * expert-contiguous buffer ("CuTeDSL at Perplexity", local MoE dispatch /
+ * combine kernel: counting, unique index per token, copy into the buffers
+ * that feed the MoE GEMM; prefill routing split over blocks with per-block
+ * counters accumulated in global memory).
+ * The order is deterministic and stable: inside expert e's segment, rows are
+ * in ascending token id.  Segments are unpadded.
+ *
+ *   idx      : int32 [T, k]   expert of each slot (0 <= idx < E, distinct per token)
+ *   x_rows   : [T, row_bytes] token rows (bf16 row: 2H bytes; NVFP4 row: H/2
+ *              bytes); may be NULL when xp_rows is NULL
+ *   x_sf     : [T, sf_row_bytes] per-row scale bytes copied alongside (NVFP4
+ *              rows: H/16 bytes), or NULL
+ *   counts   : int32 [E]      slots routed to each expert
+ *   offsets  : int32 [E+1]    exclusive prefix sum of counts; offsets[E] = T*k
+ *   row_of   : int32 [T, k]   row of slot (t, j) in the permuted buffer
+ *   src_tok  : int32 [T*k]    token of each permuted row
+ *   xp_rows  : [T*k, row_bytes] permuted rows (NULL: metadata only)
+ *   xp_sf    : [T*k, sf_row_bytes] permuted scale rows (NULL if x_sf is NULL)
+ * row_bytes must be a positive multiple of 16; sf_row_bytes a positive
+ * multiple of 4 (when x_sf is given); pointers 16-byte aligned.
+ * E <= 4096.  Workspace: moe_permute_workspace_size(T, k, E). */
+size_t moe_permute_workspace_size(int T, int k, int E);
+int moe_permute(const int32_t* idx, int T, int k, int E,
+                const void* x_rows, int row_bytes,
+                const uint8_t* x_sf, int sf_row_bytes,
+                int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
+                void* xp_rows, uint8_t* xp_sf,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ quant_nvfp4
+ * NVFP4 quantisation of bf16 matrices (activations before dispatch:
+ * "Driving vLLM WideEP ... (Part I)", section "NVFP4 MoE dispatch"; abs-max
+ * over 16 elements: "CuTeDSL at Perplexity", Blackwell support).
+ * Recipe, in IEEE fp32 with round-to-nearest-even:
+ *   g   = amax(|x|) / 2688 per group (1 if the group is all zero), unless g_in
+ *   s_b = E4M3_satfinite(amax_b / (6 g))           per 16 elements of a row
+ *   q_i = E2M1_satfinite(x_i / (e4m3(s_b) g))      magnitude 0 if e4m3(s_b) == 0
+ * Ties round to the even code; the code's sign bit is the sign of x_i.
+ *
+ *   x      : bf16 [groups, rows, cols]
+ *   g_in   : fp32 [groups] device, or NULL to derive g from each group's amax
+ *   codes  : uint8 [groups, rows, cols/2]
+ *   sf     : uint8 [groups, rows, cols/16] (E4M3)
+ *   g_out  : fp32 [groups] device (required; receives g)
+ * cols must be a multiple of 16.  Workspace:
+ * moe_quant_nvfp4_workspace_size(groups). */
+size_t moe_quant_nvfp4_workspace_size(int groups);
+int moe_quant_nvfp4(const uint16_t* x, int groups, int rows, int cols,
+                    const float* g_in, uint8_t* codes, uint8_t* sf, float* g_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ grouped GEMM
+ * Expert GEMMs over expert-contiguous rows ("Hosting Qwen on Blackwell",
+ * section "MoE GEMM"; NVFP4 weights dequantised inside the MMA path:
+ * "Driving vLLM WideEP ... (Part I)", section "NVFP4 GEMM for MoE and
+ * O-proj").  For every group g and every row r in [offsets[g], offsets[g+1]):
+ *   STORE_BF16  : C[r, :N]  = bf16( a_g w_g[g] * sum_k A[r,k] W[g,n,k] )
+ *   SWIGLU_*    : G = A W[g, 0:N]^T, U = A W[g, N:2N]^T (scaled likewise),
+ *                 C[r, :N] = silu(G) * U  (bf16, or NVFP4 with global scale *c_g)
+ * Operand formats: A bf16 [M_total, K] or NVFP4 (A = codes [M_total, K/2],
+ * A_sf [M_total, K/16], *A_g); W bf16 [G, Wn, K] or NVFP4 (W_sf
+ * [G, Wn, K/16], W_g [G]); Wn = N (STORE) or 2N (SWIGLU).  Scale pointers
+ * (A_g, W_g, c_g) are device pointers; pass NULL for bf16 operands.
+ * SWIGLU_NVFP4 writes C = codes [M_total, N/2] and C_sf [M_total, N/16].
+ * The kernel is persistent (one CTA per SM), reads offsets on the device,
+ * stages tiles with TMA into shared memory, and runs tcgen05 MMAs with
+ * fp32 accumulators in tensor memory.
+ * Requirements: K % 64 == 0, N % 32 == 0, G <= 1024, M_total < 2^31,
+ * offsets non-decreasing with offsets[G] <= M_total; A and W 16-byte aligned.
+ */
+int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue,
+                     int G, const int32_t* offsets, int M_total, int N, int K,
+                     const void* A, const uint8_t* A_sf, const float* A_g,
+                     const void* W, const uint8_t* W_sf, const float* W_g,
+                     void* C, uint8_t* C_sf, const float* c_g,
+                     void* stream);
+
+/* ----------------------------------------------------------------- combine
+ * Weighted unpermute ("CuTeDSL at Perplexity", combine kernel: vectorised
+ * accumulation in registers using the token positions from dispatch):
+ *   out[t, :] = bf16( sum_{j<k} w[t,j] * Y[row_of[t,j], :]  (+ Ys[t, :]) )
+ * accumulated in fp32 in the order j = 0..k-1, then the shared expert row.
+ *   Y  : bf16 [T*k, H]   expert outputs in permuted order
+ *   Ys : bf16 [T, H]     shared expert output, or NULL
+ *   out: bf16 [T, H]
+ * H must be a multiple of 8; pointers 16-byte aligned. */
+int moe_combine(const uint16_t* Y, const int32_t* row_of, const float* w,
+                const uint16_t* Ys, int T, int k, int H,
+                uint16_t* out, void* stream);
+
+/* ----------------------------------------------------------- whole layer
+ * Weight description of one layer.  All pointers are device pointers.
+ *   bf16 weights : w13 [E, 2I, H] (rows [0,I) gate, [I,2I) up), w2 [E, H, I],
+ *                  ws13 [2I_s, H], ws2 [H, I_s]; *_sf and *_g NULL
+ *   NVFP4 weights: w13 codes [E, 2I, H/2], w13_sf [E, 2I, H/16], w13_g [E];
+ *                  w2 codes [E, H, I/2], w2_sf [E, H, I/16], w2_g [E];
+ *                  shared likewise with one global scale each
+ *   act_fmt NVFP4 (requires w_fmt NVFP4): x is quantised to NVFP4 (one global
+ *                  scale over x) before dispatch, and the SwiGLU output h is
+ *                  quantised to NVFP4 with the caller's global scales
+ *                  *g_h (routed) and *g_hs (shared) before the down GEMM.
+ * I_s = 0 means no shared expert. */
+typedef struct {
+  int H, E, k, I, I_s;
+  int w_fmt, act_fmt;
+  const void* w13; const uint8_t* w13_sf; const float* w13_g;
+  const void* w2;  const uint8_t* w2_sf;  const float* w2_g;
+  const void* ws13; const uint8_t* ws13_sf; const float* ws13_g;
+  const void* ws2;  const uint8_t* ws2_sf;  const float* ws2_g;
+  const float* g_h;
+  const float* g_hs;
+} moe_layer;
+
+/* Workspace bytes moe_forward needs for T tokens (0 on invalid layer). */
+size_t moe_forward_workspace_size(const moe_layer* L, int T);
+
+/* The whole layer: route -> (NVFP4 activation quantisation) -> permute ->
+ * grouped GEMM gate/up + SwiGLU -> grouped GEMM down -> combine, with the
+ * shared expert folded into both grouped GEMM launches.
+ *   x      : bf16 [T, H]
+ *   logits : fp32 [T, E]
+ *   out    : bf16 [T, H]
+ * Constraints: those of each stage (H % 64 == 0, I % 64 == 0, I_s % 64 == 0,
+ * k <= 32, E <= 1024). */
+int moe_forward(const moe_layer* L, const uint16_t* x, const float* logits, int T,
+                uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward that also records caller-created CUDA events (cudaEvent_t
+ * passed as void*) on `stream` at the stage boundaries, for live per-stage
+ * timing: events[0] before routing, [1] after routing, [2] after the NVFP4
+ * activation quantisation (nothing is launched there on bf16 activations),
+ * [3] after the permutation, [4] after the gate/up grouped GEMM, [5] after
+ * the down grouped GEMM, [6] after the combine.  `events` may be NULL, and
+ * any entry may be NULL to skip it.  Launches exactly the kernels of
+ * moe_forward. */
+int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const float* logits, int T,
+                         uint16_t* out, void* ws, size_t ws_bytes, void* const* events,
+                         void* stream);
+
+/* moe_forward with HOST inputs and output: copies x_host (bf16 [T,H]) and
+ * logits_host (fp32 [T,E]) into the caller's device buffers x_dev and
+ * logits_dev, runs the layer, copies the result into out_host (bf16 [T,H])
+ * through out_dev, and synchronises `stream`.  Host buffers should be pinned
+ * for asynchronous copies. */
+int moe_forward_host(const moe_layer* L, const uint16_t* x_host, const float* logits_host,
+                     int T, uint16_t* out_host,
+                     uint16_t* x_dev, float* logits_dev, uint16_t* out_dev,
+                     void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,192 @@
+"""Python binding of the C ABI (include/moe_gb300.h), same names.
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+PyTorch provides device memory and the current stream.  Outputs that are not
+passed in are allocated with torch on the input's device.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import (MOE_EPI_STORE_BF16, MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_NVFP4, MOE_FMT_BF16,
+                   MOE_FMT_NVFP4, check, load)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev(t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    # 256-byte aligned by the caching allocator (allocations are 512-byte aligned)
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def moe_version() -> int:
+    return load().moe_version()
+
+
+def moe_sync_status(stream=None) -> int:
+    return load().moe_sync_status(_stream(stream))
+
+
+def moe_set_wait_timeout_ns(ns: int) -> None:
+    check(load().moe_set_wait_timeout_ns(int(ns)), "moe_set_wait_timeout_ns")
+
+
+def moe_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    check(load().moe_selftest_wait_timeout(int(timeout_ns), _stream(stream)), "moe_selftest_wait_timeout")
+
+
+def moe_route(logits: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
+              w: Optional[torch.Tensor] = None, stream=None):
+    """logits fp32 [T, E] -> (idx int32 [T, k], w fp32 [T, k])."""
+    _dev(logits)
+    assert logits.dtype == torch.float32 and logits.dim() == 2
+    T, E = logits.shape
+    if idx is None:
+        idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    if w is None:
+        w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    check(load().moe_route(_ptr(logits), T, E, k, _ptr(idx), _ptr(w), _stream(stream)), "moe_route")
+    return idx, w
+
+
+def moe_permute(idx: torch.Tensor, E: int, x_rows: Optional[torch.Tensor] = None,
+                x_sf: Optional[torch.Tensor] = None, stream=None):
+    """Stable permutation into expert-contiguous order.
+
+    idx int32 [T, k]; x_rows: [T, ...] any dtype (rows copied as bytes) or None;
+    x_sf: uint8 [T, sf_bytes] or None.  Returns dict(counts, offsets, row_of,
+    src_tok, xp, xp_sf)."""
+    _dev(idx)
+    T, k = idx.shape
+    dev = idx.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = torch.empty(T, k, dtype=torch.int32, device=dev)
+    src_tok = torch.empty(T * k, dtype=torch.int32, device=dev)
+    xp = xp_sf = None
+    row_bytes = sf_bytes = 0
+    if x_rows is not None:
+        _dev(x_rows)
+        row_bytes = x_rows[0].numel() * x_rows.element_size() if T else 0
+        xp = torch.empty((T * k,) + tuple(x_rows.shape[1:]), dtype=x_rows.dtype, device=dev)
+        if x_sf is not None:
+            _dev(x_sf)
+            sf_bytes = x_sf.shape[1]
+            xp_sf = torch.empty(T * k, sf_bytes, dtype=torch.uint8, device=dev)
+    lib = load()
+    nbytes = lib.moe_permute_workspace_size(T, k, E)
+    ws = _ws(nbytes, dev)
+    check(lib.moe_permute(_ptr(idx), T, k, E, _ptr(x_rows), row_bytes, _ptr(x_sf), sf_bytes,
+                          _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_tok), _ptr(xp),
+                          _ptr(xp_sf), _ptr(ws), nbytes, _stream(stream)), "moe_permute")
+    return dict(counts=counts, offsets=offsets, row_of=row_of, src_tok=src_tok, xp=xp, xp_sf=xp_sf)
+
+
+def moe_quant_nvfp4(x: torch.Tensor, g_in: Optional[torch.Tensor] = None, stream=None):
+    """x bf16 [rows, cols] or [groups, rows, cols] -> (codes uint8 [..., cols/2],
+    sf uint8 [..., cols/16], g fp32 [groups])."""
+    _dev(x)
+    assert x.dtype == torch.bfloat16
+    x3 = x if x.dim() == 3 else x.unsqueeze(0)
+    G, R, Cc = x3.shape
+    codes = torch.empty(x.shape[:-1] + (Cc // 2,), dtype=torch.uint8, device=x.device)
+    sf = torch.empty(x.shape[:-1] + (Cc // 16,), dtype=torch.uint8, device=x.device)
+    g = torch.empty(G, dtype=torch.float32, device=x.device)
+    lib = load()
+    nbytes = lib.moe_quant_nvfp4_workspace_size(G)
+    ws = _ws(nbytes, x.device)
+    check(lib.moe_quant_nvfp4(_ptr(x3), G, R, Cc, _ptr(g_in), _ptr(codes), _ptr(sf), _ptr(g),
+                              _ptr(ws), nbytes, _stream(stream)), "moe_quant_nvfp4")
+    return codes, sf, g
+
+
+def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tensor, N: int, K: int,
+                     A: torch.Tensor, W: torch.Tensor, A_sf=None, A_g=None, W_sf=None, W_g=None,
+                     c_g=None, C=None, C_sf=None, stream=None):
+    """Grouped GEMM over expert-contiguous rows; see include/moe_gb300.h."""
+    _dev(offsets)
+    G = offsets.numel() - 1
+    M = A.shape[0]
+    dev = A.device
+    if C is None:
+        if epilogue == MOE_EPI_SWIGLU_NVFP4:
+            C = torch.empty(M, N // 2, dtype=torch.uint8, device=dev)
+            C_sf = torch.empty(M, N // 16, dtype=torch.uint8, device=dev)
+        else:
+            C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    check(load().moe_grouped_gemm(a_fmt, w_fmt, epilogue, G, _ptr(offsets), M, N, K, _ptr(A), _ptr(A_sf),
+                                  _ptr(A_g), _ptr(W), _ptr(W_sf), _ptr(W_g), _ptr(C), _ptr(C_sf), _ptr(c_g),
+                                  _stream(stream)), "moe_grouped_gemm")
+    return (C, C_sf) if epilogue == MOE_EPI_SWIGLU_NVFP4 else C
+
+
+def moe_combine(Y: torch.Tensor, row_of: torch.Tensor, w: torch.Tensor, Ys: Optional[torch.Tensor],
+                T: int, k: int, H: int, out: Optional[torch.Tensor] = None, stream=None):
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=Y.device)
+    check(load().moe_combine(_ptr(Y), _ptr(row_of), _ptr(w), _ptr(Ys), T, k, H, _ptr(out), _stream(stream)),
+          "moe_combine")
+    return out
+
+
+def moe_forward_workspace_size(layer_c, T: int) -> int:
+    import ctypes
+    return int(load().moe_forward_workspace_size(ctypes.byref(layer_c), T))
+
+
+def moe_forward(layer_c, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                stream=None) -> torch.Tensor:
+    import ctypes
+    T = x.shape[0]
+    check(load().moe_forward(ctypes.byref(layer_c), _ptr(x), _ptr(logits), T, _ptr(out), _ptr(ws),
+                             ws.numel(), _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_forward_profiled(layer_c, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                         events, stream=None) -> torch.Tensor:
+    """moe_forward recording 7 torch.cuda.Event objects at the stage
+    boundaries (see include/moe_gb300.h)."""
+    import ctypes
+    assert len(events) == 7
+    handles = (ctypes.c_void_p * 7)(*[ev.cuda_event for ev in events])
+    T = x.shape[0]
+    check(load().moe_forward_profiled(ctypes.byref(layer_c), _ptr(x), _ptr(logits), T, _ptr(out), _ptr(ws),
+                                      ws.numel(), handles, _stream(stream)), "moe_forward_profiled")
+    return out
+
+
+def moe_forward_host(layer_c, x_host: torch.Tensor, logits_host: torch.Tensor, out_host: torch.Tensor,
+                     x_dev: torch.Tensor, logits_dev: torch.Tensor, out_dev: torch.Tensor,
+                     ws: torch.Tensor, stream=None) -> torch.Tensor:
+    import ctypes
+    T = x_host.shape[0]
+    check(load().moe_forward_host(ctypes.byref(layer_c), _ptr(x_host), _ptr(logits_host), T, _ptr(out_host),
+                                  _ptr(x_dev), _ptr(logits_dev), _ptr(out_dev), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "moe_forward_host")
+    return out_host
+
+
+__all__ = ["MOE_FMT_BF16", "MOE_FMT_NVFP4", "MOE_EPI_STORE_BF16", "MOE_EPI_SWIGLU_BF16",
+           "MOE_EPI_SWIGLU_NVFP4", "moe_version", "moe_sync_status", "moe_set_wait_timeout_ns",
+           "moe_selftest_wait_timeout", "moe_route", "moe_permute", "moe_quant_nvfp4",
+           "moe_grouped_gemm", "moe_combine", "moe_forward_workspace_size", "moe_forward",
+           "moe_forward_profiled", "moe_forward_host"]

@@ -1,0 +1,128 @@
+// Library-wide host plumbing: version, status strings, CUDA error capture,
+// the device error word of the bounded waits, and the wait time-out hook.
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace moe {
+
+static char g_last_err[256] = "no error";
+static unsigned long long g_timeout_ns = 1000000000ull;
+
+// One error word per device, set by bounded device waits that run out.
+__device__ unsigned int g_err_word;
+
+void set_cuda_error(cudaError_t e) {
+  snprintf(g_last_err, sizeof(g_last_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int check_launch() {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns; }
+
+unsigned int* device_error_word() {
+  static unsigned int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_err_word);
+    if (e != cudaSuccess) {
+      set_cuda_error(e);
+      return nullptr;
+    }
+    cache[dev] = static_cast<unsigned int*>(p);
+  }
+  return cache[dev];
+}
+
+__global__ void selftest_wait_kernel(unsigned int* err, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on `bar`: the bounded wait must give up and record it
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, timeout_ns, err, nullptr);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+const char* moe_last_cuda_error(void) { return g_last_err; }
+
+int moe_set_wait_timeout_ns(unsigned long long ns) {
+  g_timeout_ns = ns ? ns : 1000000000ull;
+  return MOE_OK;
+}
+
+int moe_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_err_word, sizeof(v));
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  if (v != 0) {
+    unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) {
+      set_cuda_error(e);
+      return MOE_ERR_CUDA;
+    }
+    return MOE_ERR_TIMEOUT;
+  }
+  return MOE_OK;
+}
+
+int moe_selftest_wait_timeout(unsigned long long timeout_ns, void* stream) {
+  unsigned int* err = device_error_word();
+  if (!err) return MOE_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, timeout_ns);
+  return check_launch();
+}
+
+}  // extern "C"

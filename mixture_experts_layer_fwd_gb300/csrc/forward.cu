@@ -1,0 +1,207 @@
+// The whole layer: route -> (NVFP4 activation quantisation) -> permute ->
+// grouped GEMM gate/up + SwiGLU -> grouped GEMM down -> combine, all
+// stream-ordered on the caller's stream with no host synchronisation.
+//
+// Step order follows the pages: routing table, local dispatch into expert
+// buffers, MoE GEMM, weighted combine ("CuTeDSL at Perplexity", local
+// dispatch / combine; "Hosting Qwen on Blackwell", sections "MoE Dispatch -
+// Combine" and "MoE GEMM"); activations are quantised to NVFP4 before
+// dispatch ("Driving vLLM WideEP ... (Part I)", section "NVFP4 MoE
+// dispatch").  The shared expert is folded into both grouped GEMM launches
+// as one more group over all T tokens.
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+struct FwdBufs {
+  int32_t* idx;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_of;
+  int32_t* src_tok;
+  void* perm_ws;
+  size_t perm_ws_bytes;
+  uint8_t* xq;
+  uint8_t* xsf;
+  float* gx;
+  void* qws;
+  void* xp;
+  uint8_t* xp_sf;
+  void* h;
+  uint8_t* h_sf;
+  void* hs;
+  uint8_t* hs_sf;
+  uint16_t* Y;
+  uint16_t* Ys;
+};
+
+int validate_layer(const moe_layer* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (L->H < 1 || L->E < 1 || L->k < 1 || L->I < 1 || L->I_s < 0) return MOE_ERR_INVALID_ARG;
+  if (L->k > L->E || L->k > 32 || L->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (L->H % 64 || L->I % 64 || L->I_s % 64) return MOE_ERR_UNSUPPORTED;
+  const bool w4 = L->w_fmt == MOE_FMT_NVFP4, a4 = L->act_fmt == MOE_FMT_NVFP4;
+  if (L->w_fmt != MOE_FMT_BF16 && !w4) return MOE_ERR_INVALID_ARG;
+  if (L->act_fmt != MOE_FMT_BF16 && !a4) return MOE_ERR_INVALID_ARG;
+  if (a4 && !w4) return MOE_ERR_UNSUPPORTED;
+  if (!L->w13 || !L->w2) return MOE_ERR_INVALID_ARG;
+  if (w4 && (!L->w13_sf || !L->w13_g || !L->w2_sf || !L->w2_g)) return MOE_ERR_INVALID_ARG;
+  if (L->I_s) {
+    if (!L->ws13 || !L->ws2) return MOE_ERR_INVALID_ARG;
+    if (w4 && (!L->ws13_sf || !L->ws13_g || !L->ws2_sf || !L->ws2_g)) return MOE_ERR_INVALID_ARG;
+  }
+  if (a4 && (!L->g_h || (L->I_s && !L->g_hs))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Lays the buffers out in the workspace (ws may be null to size it).
+size_t carve(const moe_layer* L, int T, void* ws, size_t cap, FwdBufs* b) {
+  const size_t Tk = static_cast<size_t>(T) * L->k;
+  const bool a4 = L->act_fmt == MOE_FMT_NVFP4;
+  Carve c(ws, cap);
+  b->idx = c.take<int32_t>(Tk);
+  b->w = c.take<float>(Tk);
+  b->counts = c.take<int32_t>(L->E);
+  b->offsets = c.take<int32_t>(L->E + 1);
+  b->row_of = c.take<int32_t>(Tk);
+  b->src_tok = c.take<int32_t>(Tk);
+  b->perm_ws_bytes = permute_ws_bytes(T, L->k, L->E);
+  b->perm_ws = c.take<uint8_t>(b->perm_ws_bytes);
+  b->xq = b->xsf = nullptr;
+  b->gx = nullptr;
+  b->qws = nullptr;
+  b->xp_sf = b->h_sf = b->hs_sf = nullptr;
+  b->hs = nullptr;
+  b->Ys = nullptr;
+  if (a4) {
+    b->xq = c.take<uint8_t>(static_cast<size_t>(T) * L->H / 2);
+    b->xsf = c.take<uint8_t>(static_cast<size_t>(T) * L->H / 16);
+    b->gx = c.take<float>(1);
+    b->qws = c.take<uint8_t>(quant_ws_bytes(1));
+    b->xp = c.take<uint8_t>(Tk * L->H / 2);
+    b->xp_sf = c.take<uint8_t>(Tk * L->H / 16);
+    b->h = c.take<uint8_t>(Tk * L->I / 2);
+    b->h_sf = c.take<uint8_t>(Tk * L->I / 16);
+    if (L->I_s) {
+      b->hs = c.take<uint8_t>(static_cast<size_t>(T) * L->I_s / 2);
+      b->hs_sf = c.take<uint8_t>(static_cast<size_t>(T) * L->I_s / 16);
+    }
+  } else {
+    b->xp = c.take<uint16_t>(Tk * L->H);
+    b->h = c.take<uint16_t>(Tk * L->I);
+    if (L->I_s) b->hs = c.take<uint16_t>(static_cast<size_t>(T) * L->I_s);
+  }
+  b->Y = c.take<uint16_t>(Tk * L->H);
+  if (L->I_s) b->Ys = c.take<uint16_t>(static_cast<size_t>(T) * L->H);
+  return c.used;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_forward_workspace_size(const moe_layer* L, int T) {
+  if (validate_layer(L) != MOE_OK || T < 0) return 0;
+  FwdBufs b;
+  return carve(L, T, nullptr, 0, &b);
+}
+
+extern "C" int moe_route(const float* logits, int T, int E, int k, int32_t* idx, float* w, void* stream);
+
+namespace {
+inline int mark(void* const* events, int i, cudaStream_t s) {
+  if (events == nullptr || events[i] == nullptr) return MOE_OK;
+  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+}  // namespace
+
+extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const float* logits, int T, uint16_t* out,
+                                    void* ws, size_t ws_bytes, void* const* events, void* stream);
+
+extern "C" int moe_forward(const moe_layer* L, const uint16_t* x, const float* logits, int T, uint16_t* out, void* ws,
+                           size_t ws_bytes, void* stream) {
+  return moe_forward_profiled(L, x, logits, T, out, ws, ws_bytes, nullptr, stream);
+}
+
+extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const float* logits, int T, uint16_t* out,
+                                    void* ws, size_t ws_bytes, void* const* events, void* stream) {
+  MOE_TRY(validate_layer(L));
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !logits || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(logits, 4) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * L->k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  FwdBufs b;
+  if (carve(L, T, ws, ws_bytes, &b) > ws_bytes) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool a4 = L->act_fmt == MOE_FMT_NVFP4;
+  const int H = L->H, E = L->E, k = L->k;
+  const int Tk = T * k;
+
+  MOE_TRY(mark(events, 0, s));
+  MOE_TRY(moe_route(logits, T, E, k, b.idx, b.w, stream));
+  MOE_TRY(mark(events, 1, s));
+  if (a4) MOE_TRY(quant_launch(x, 1, T, H, nullptr, b.xq, b.xsf, b.gx, b.qws, quant_ws_bytes(1), s));
+  MOE_TRY(mark(events, 2, s));
+  if (a4)
+    MOE_TRY(permute_launch(b.idx, T, k, E, b.xq, H / 2, b.xsf, H / 16, b.counts, b.offsets, b.row_of, b.src_tok, b.xp,
+                           b.xp_sf, b.perm_ws, b.perm_ws_bytes, s));
+  else
+    MOE_TRY(permute_launch(b.idx, T, k, E, x, H * 2, nullptr, 0, b.counts, b.offsets, b.row_of, b.src_tok, b.xp,
+                           nullptr, b.perm_ws, b.perm_ws_bytes, s));
+
+  MOE_TRY(mark(events, 3, s));
+
+  // gate/up projection + SwiGLU (routed groups + shared expert)
+  const int epi1 = a4 ? MOE_EPI_SWIGLU_NVFP4 : MOE_EPI_SWIGLU_BF16;
+  GemmProblem r1{b.xp, b.xp_sf, b.gx, Tk, L->w13, L->w13_sf, L->w13_g, E, b.h, b.h_sf, L->g_h, L->I, H};
+  GemmProblem s1{a4 ? static_cast<const void*>(b.xq) : static_cast<const void*>(x),
+                 b.xsf, b.gx, T, L->ws13, L->ws13_sf, L->ws13_g, 1, b.hs, b.hs_sf, L->g_hs, L->I_s, H};
+  MOE_TRY(grouped_gemm_launch(epi1, L->act_fmt, L->w_fmt, r1, b.offsets, E, L->I_s ? &s1 : nullptr, T, s));
+
+  MOE_TRY(mark(events, 4, s));
+
+  // down projection
+  GemmProblem r2{b.h, b.h_sf, L->g_h, Tk, L->w2, L->w2_sf, L->w2_g, E, b.Y, nullptr, nullptr, H, L->I};
+  GemmProblem s2{b.hs, b.hs_sf, L->g_hs, T, L->ws2, L->ws2_sf, L->ws2_g, 1, b.Ys, nullptr, nullptr, H, L->I_s};
+  MOE_TRY(grouped_gemm_launch(MOE_EPI_STORE_BF16, L->act_fmt, L->w_fmt, r2, b.offsets, E, L->I_s ? &s2 : nullptr, T,
+                              s));
+
+  MOE_TRY(mark(events, 5, s));
+  MOE_TRY(combine_launch(b.Y, b.row_of, b.w, b.Ys, T, k, H, out, s));
+  return mark(events, 6, s);
+}
+
+extern "C" int moe_forward_host(const moe_layer* L, const uint16_t* x_host, const float* logits_host, int T,
+                                uint16_t* out_host, uint16_t* x_dev, float* logits_dev, uint16_t* out_dev, void* ws,
+                                size_t ws_bytes, void* stream) {
+  MOE_TRY(validate_layer(L));
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !logits_host || !out_host || !x_dev || !logits_dev || !out_dev) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = static_cast<size_t>(T) * L->H * sizeof(uint16_t);
+  const size_t lb = static_cast<size_t>(T) * L->E * sizeof(float);
+  cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(logits_dev, logits_host, lb, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  MOE_TRY(moe_forward(L, x_dev, logits_dev, T, out_dev, ws, ws_bytes, stream));
+  e = cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return moe_sync_status(stream);
+}

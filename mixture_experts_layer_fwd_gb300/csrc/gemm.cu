@@ -1,0 +1,616 @@
+// Persistent grouped GEMM for the expert projections on sm_103a.
+//
+// "Hosting Qwen on Blackwell", section "MoE GEMM": every expert multiplies its
+// group of routed tokens by its weights; dense at prefill (hundreds of tokens
+// per expert), weight-load bound at decode (section "Decodificadores").
+// "Driving vLLM WideEP ... (Part I)", section "NVFP4 GEMM for MoE and
+// O-proj": NVFP4 weights (packed 4-bit values + per-group FP8 scales) are
+// dequantised on the fly inside the GEMM.
+//
+// Design (one CTA per SM, warp-specialised):
+//   warp 0      TMA producer: A tile 128 rows x 64 K (bf16, 128-byte swizzle)
+//               and B tile 256 rows x 64 K per pipeline stage, mbarrier
+//               complete_tx; NVFP4 operands arrive as packed codes instead
+//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
+//               M=128 N=256 K=16, fp32 accumulators in tensor memory, two
+//               accumulator buffers of 256 columns (epilogue of tile i
+//               overlaps the main loop of tile i+1)
+//   warps 2..5  epilogue: tcgen05.ld of the accumulators, SwiGLU / scaling /
+//               bf16 or NVFP4 rounding, stores of the rows of the tile that
+//               belong to the tile's group
+//   warps 6..9  (NVFP4 operands only) converters: packed E2M1 codes x E4M3
+//               scale -> bf16 into the swizzled operand tile.  e2m1 * e4m3 is
+//               exact in bf16, so the bf16 MMA computes exactly the NVFP4
+//               products; the fp32 global scales are applied in the epilogue.
+// Tiles are (group, n-block, m-block) with m fastest; group sizes are read
+// on the device (offsets), so nothing is synchronised with the host.
+// The SwiGLU epilogue needs gate and up of the same feature in one thread:
+// the B tile holds 128 gate rows followed by the matching 128 up rows, so
+// accumulator columns [0,128) are gate and [128,256) are up.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "internal.h"
+#include "nvfp4.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int TMEM_COLS = 512;
+constexpr int A_TILE = BM * BK * 2;   // 16 KB bf16
+constexpr int B_TILE = BN * BK * 2;   // 32 KB bf16
+constexpr int A_CODES = BM * BK / 2;  // 4 KB packed E2M1
+constexpr int B_CODES = BN * BK / 2;  // 8 KB packed E2M1
+constexpr int MAX_G = 1025;  // routed groups + the shared expert
+
+struct Prob {
+  int n_out;         // output columns N
+  int K;             // reduction length
+  int w_rows;        // weight rows per group (N, or 2N for SwiGLU)
+  int n_tiles;       // column blocks per group
+  int a_rows;        // rows of A (bounds of the scale loads)
+  int w_rows_total;  // rows of W over all groups
+  void* c;
+  uint8_t* c_sf;
+  const float* a_g;
+  const float* w_g;
+  const float* c_g;
+  const uint8_t* a_sf;
+  const uint8_t* w_sf;
+};
+
+struct Params {
+  CUtensorMap tma_a[2];  // [0] routed problem, [1] shared-expert problem
+  CUtensorMap tma_w[2];
+  Prob prob[2];
+  const int32_t* offsets;  // [G+1] rows of each routed group in A
+  int G;
+  int shared_rows;  // rows of the shared problem; < 0: none
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+template <int EPI, bool A4, bool W4>
+struct Cfg {
+  static constexpr bool CONV = A4 || W4;
+  static constexpr int STAGES = CONV ? 3 : 4;
+  static constexpr int STAGE_BYTES = A_TILE + B_TILE + (A4 ? A_CODES : 0) + (W4 ? B_CODES : 0);
+  static constexpr int NUM_WARPS = CONV ? 10 : 6;
+  static constexpr int THREADS = NUM_WARPS * 32;
+  static constexpr int TILE_N = (EPI == MOE_EPI_STORE_BF16) ? 256 : 128;  // output columns per tile
+  static constexpr uint32_t TX_BYTES = (A4 ? A_CODES : A_TILE) + (W4 ? B_CODES : B_TILE);
+  static constexpr int EXTRA = 2048 + 4 * (2 * MAX_G + 8) + 1024;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA;
+  static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct TileInfo {
+  int pb;     // problem: 0 routed, 1 shared
+  int g;      // group inside the problem
+  int row0;   // first row of the group in A / C
+  int rows;   // rows of the group
+  int m_blk;  // row block inside the group
+  int n_blk;  // column block
+};
+
+DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
+  int lo = 0, hi = GT;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  const bool routed = lo < G;
+  ti.pb = routed ? 0 : 1;
+  ti.g = routed ? lo : 0;
+  ti.row0 = routed ? s_off[lo] : 0;
+  ti.rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
+  const int mt = (ti.rows + BM - 1) / BM;
+  const int local = t - s_prefix[lo];
+  ti.n_blk = local / mt;
+  ti.m_blk = local - ti.n_blk * mt;
+  return ti;
+}
+
+DEVINL float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// Converts one 64-element row of packed E2M1 codes (32 bytes in smem) with
+// its four E4M3 block scales into bf16, written into a 128-byte swizzled row.
+DEVINL void convert_row(const uint8_t* codes, uint32_t sfw, uint8_t* tile, int row, const uint32_t* lut) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(codes);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(codes + 16);
+  const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const float sc = e4m3_decode((sfw >> (8 * (ch >> 1))) & 0xFFu);
+    const __nv_bfloat162 s2 = __float2bfloat162_rn(sc);
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t lv = lut[(cw[ch] >> (8 * q)) & 0xFFu];
+      __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&lv);
+      v = __hmul2(v, s2);
+      o[q] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <int EPI, bool A4, bool W4>
+__global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<EPI, A4, W4>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = base;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + S * C::STAGE_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* conv = empty + S;
+  uint64_t* tfull = conv + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_prefix = reinterpret_cast<int*>(base + S * C::STAGE_BYTES + 256);
+  int* s_off = s_prefix + MAX_G + 4;
+  uint32_t* lut = reinterpret_cast<uint32_t*>(s_off + MAX_G + 4);
+  __shared__ int warp_sums[32];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.G;
+  const int GT = G + (p.shared_rows >= 0 ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&conv[s], 128);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  // ---- tile schedule: prefix over per-group tile counts
+  for (int i = threadIdx.x; i <= G; i += C::THREADS) s_off[i] = p.offsets[i];
+  if (C::CONV) {
+    for (int b = threadIdx.x; b < 256; b += C::THREADS)
+      lut[b] = e2m1_to_bf16_bits(b & 15u) | (e2m1_to_bf16_bits(b >> 4) << 16);
+  }
+  __syncthreads();
+  {
+    const int per = (GT + C::THREADS - 1) / C::THREADS;
+    const int g0 = threadIdx.x * per;
+    int local = 0;
+    for (int g = g0; g < min(GT, g0 + per); ++g) {
+      const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
+      local += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int v = (lane < C::NUM_WARPS) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (lane >= off) v += o;
+      }
+      warp_sums[lane] = v;
+    }
+    __syncthreads();
+    int run = incl - local + (warp ? warp_sums[warp - 1] : 0);
+    for (int g = g0; g < min(GT, g0 + per); ++g) {
+      s_prefix[g] = run;
+      const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
+      run += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
+    }
+    if (threadIdx.x == 0) s_prefix[GT] = warp_sums[C::NUM_WARPS - 1];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = s_prefix[GT];
+  const unsigned long long tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tma_a[0]);
+      tma_prefetch_desc(&p.tma_w[0]);
+      if (p.shared_rows >= 0) {
+        tma_prefetch_desc(&p.tma_a[1]);
+        tma_prefetch_desc(&p.tma_w[1]);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[S];
+#pragma unroll
+      for (int s = 0; s < S; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const Prob& P = p.prob[ti.pb];
+        const void* ta = &p.tma_a[ti.pb];
+        const void* tw = &p.tma_w[ti.pb];
+        const int a_y = ti.row0 + ti.m_blk * BM;
+        const int w_y0 = ti.g * P.w_rows + ti.n_blk * C::TILE_N;
+        const int w_y1 = (EPI == MOE_EPI_STORE_BF16) ? w_y0 + 128 : w_y0 + P.n_out;
+        const int nk = P.K / BK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sb = stages + stage * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::TX_BYTES);
+          if (A4)
+            tma_load_2d(ta, &full[stage], sb + A_TILE + B_TILE, kb * (BK / 2), a_y);
+          else
+            tma_load_2d(ta, &full[stage], sb, kb * BK, a_y);
+          if (W4) {
+            uint8_t* wc = sb + A_TILE + B_TILE + (A4 ? A_CODES : 0);
+            tma_load_2d(tw, &full[stage], wc, kb * (BK / 2), w_y0);
+            tma_load_2d(tw, &full[stage], wc + B_CODES / 2, kb * (BK / 2), w_y1);
+          } else {
+            tma_load_2d(tw, &full[stage], sb + A_TILE, kb * BK, w_y0);
+            tma_load_2d(tw, &full[stage], sb + A_TILE + B_TILE / 2, kb * BK, w_y1);
+          }
+          issued[stage] += 1;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already in flight land before the block exits
+        for (int s = 0; s < S; ++s)
+          if (issued[s]) mbar_wait_bounded(&full[s], (issued[s] - 1u) & 1u, 1000000000ull, p.err, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const int nk = p.prob[ti.pb].K / BK;
+        const int buf = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        if (!mbar_wait_bounded(&tempty[buf], (use & 1u) ^ 1u, tmo, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(C::CONV ? &conv[stage] : &full[stage], phase, tmo, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stages + stage * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + A_TILE;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            umma_f16(d, smem_desc_kmajor_sw128(a_addr + kk * 32), smem_desc_kmajor_sw128(b_addr + kk * 32), IDESC,
+                     (kb | kk) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(&tfull[buf]);
+      }
+      if (!ok) {
+        umma_commit(drain);
+        mbar_wait_bounded(drain, 0, 1000000000ull, p.err, nullptr);
+      }
+    }
+  } else if (warp < 6) {
+    // ===================================================== epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const TileInfo ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const Prob& P = p.prob[ti.pb];
+      const int buf = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      if (!mbar_wait_bounded(&tfull[buf], use & 1u, tmo, p.err, abort_flag)) break;
+      tc_fence_after();
+      const int m_local = ti.m_blk * BM + r_in_tile;
+      const bool valid = m_local < ti.rows;
+      const size_t row = static_cast<size_t>(ti.row0) + m_local;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      float scale = 1.0f;
+      if (A4) scale *= __ldg(P.a_g);
+      if (W4) scale *= __ldg(P.w_g + ti.g);
+      if (EPI == MOE_EPI_STORE_BF16) {
+#pragma unroll 1
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + cc * 32, r);
+          tmem_ld_wait();
+          const int col = ti.n_blk * BN + cc * 32;
+          if (valid && col < P.n_out) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.c) + row * P.n_out + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * scale, __uint_as_float(r[8 * v + 1]) * scale);
+              o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * scale, __uint_as_float(r[8 * v + 3]) * scale);
+              o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * scale, __uint_as_float(r[8 * v + 5]) * scale);
+              o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * scale, __uint_as_float(r[8 * v + 7]) * scale);
+              dst[v] = o;
+            }
+          }
+        }
+      } else {
+        const float cg = (EPI == MOE_EPI_SWIGLU_NVFP4) ? __ldg(P.c_g) : 1.0f;
+#pragma unroll 1
+        for (int cc = 0; cc < 128 / 32; ++cc) {
+          uint32_t rg[32], ru[32];
+          tmem_ld_32x32b_x32(taddr + cc * 32, rg);
+          tmem_ld_32x32b_x32(taddr + 128 + cc * 32, ru);
+          tmem_ld_wait();
+          const int col = ti.n_blk * 128 + cc * 32;
+          if (valid && col < P.n_out) {
+            float h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              h[i] = silu_f(__uint_as_float(rg[i]) * scale) * (__uint_as_float(ru[i]) * scale);
+            if (EPI == MOE_EPI_SWIGLU_BF16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.c) + row * P.n_out + col);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[v] = make_uint4(pack_bf16x2(h[8 * v], h[8 * v + 1]), pack_bf16x2(h[8 * v + 2], h[8 * v + 3]),
+                                    pack_bf16x2(h[8 * v + 4], h[8 * v + 5]), pack_bf16x2(h[8 * v + 6], h[8 * v + 7]));
+            } else {
+              float b0[16], b1[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                b0[i] = h[i];
+                b1[i] = h[16 + i];
+              }
+              uint32_t c0[2], c1[2];
+              const uint32_t s0 = nvfp4_quantize16(b0, cg, c0);
+              const uint32_t s1 = nvfp4_quantize16(b1, cg, c1);
+              uint8_t* cdst = static_cast<uint8_t*>(P.c) + row * (P.n_out / 2) + col / 2;
+              *reinterpret_cast<uint4*>(cdst) = make_uint4(c0[0], c0[1], c1[0], c1[1]);
+              *reinterpret_cast<uint16_t*>(P.c_sf + row * (P.n_out / 16) + col / 16) =
+                  static_cast<uint16_t>(s0 | (s1 << 8));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+    }
+  } else if (C::CONV) {
+    // ===================================================== NVFP4 -> bf16 converters
+    const int ct = threadIdx.x - 6 * 32;  // 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const Prob& P = p.prob[ti.pb];
+      const int a_y = ti.row0 + ti.m_blk * BM;
+      const int w_y0 = ti.g * P.w_rows + ti.n_blk * C::TILE_N;
+      const int w_y1 = (EPI == MOE_EPI_STORE_BF16) ? w_y0 + 128 : w_y0 + P.n_out;
+      const int nk = P.K / BK;
+      const int sf_ld = P.K / 16;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase, tmo, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sb = stages + stage * C::STAGE_BYTES;
+        if (A4) {
+          const int grow = a_y + ct;
+          const uint32_t sfw =
+              (grow < P.a_rows)
+                  ? __ldg(reinterpret_cast<const uint32_t*>(P.a_sf + static_cast<size_t>(grow) * sf_ld + kb * 4))
+                  : 0u;
+          convert_row(sb + A_TILE + B_TILE + ct * 32, sfw, sb, ct, lut);
+        }
+        if (W4) {
+          const uint8_t* wc = sb + A_TILE + B_TILE + (A4 ? A_CODES : 0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int grow = (h ? w_y1 : w_y0) + ct;
+            const uint32_t sfw =
+                (grow < P.w_rows_total)
+                    ? __ldg(reinterpret_cast<const uint32_t*>(P.w_sf + static_cast<size_t>(grow) * sf_ld + kb * 4))
+                    : 0u;
+            convert_row(wc + (h * 128 + ct) * 32, sfw, sb + A_TILE, h * 128 + ct, lut);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&conv[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 2-D tensor map over a row-major [rows, inner] matrix.
+static int make_map(CUtensorMap* m, const void* ptr, bool bf16, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  const uint64_t esize = bf16 ? 2 : 1;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+}  // namespace gg
+
+template <int EPI, bool A4, bool W4>
+static int launch_impl(const gg::Params& prm, cudaStream_t s) {
+  using C = gg::Cfg<EPI, A4, W4>;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gg::grouped_gemm_kernel<EPI, A4, W4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) {
+      set_cuda_error(e);
+      return MOE_ERR_CUDA;
+    }
+    attr_done[dev] = true;
+  }
+  gg::grouped_gemm_kernel<EPI, A4, W4><<<num_sms(), C::THREADS, C::SMEM, s>>>(prm);
+  return check_launch();
+}
+
+static int fill_prob(gg::Params& prm, int slot, int epi, bool a4, bool w4, const GemmProblem& P) {
+  gg::Prob& q = prm.prob[slot];
+  const int tile_n = (epi == MOE_EPI_STORE_BF16) ? 256 : 128;
+  q.n_out = P.N;
+  q.K = P.K;
+  q.w_rows = (epi == MOE_EPI_STORE_BF16) ? P.N : 2 * P.N;
+  q.n_tiles = (P.N + tile_n - 1) / tile_n;
+  q.a_rows = P.a_rows;
+  q.w_rows_total = P.groups * q.w_rows;
+  q.c = P.C;
+  q.c_sf = P.C_sf;
+  q.a_g = P.A_g;
+  q.w_g = P.W_g;
+  q.c_g = P.c_g;
+  q.a_sf = P.A_sf;
+  q.w_sf = P.W_sf;
+  MOE_TRY(gg::make_map(&prm.tma_a[slot], P.A, !a4, a4 ? P.K / 2 : P.K, static_cast<uint64_t>(P.a_rows),
+                       a4 ? gg::BK / 2 : gg::BK, gg::BM));
+  MOE_TRY(gg::make_map(&prm.tma_w[slot], P.W, !w4, w4 ? P.K / 2 : P.K, static_cast<uint64_t>(q.w_rows_total),
+                       w4 ? gg::BK / 2 : gg::BK, 128));
+  return MOE_OK;
+}
+
+static int check_problem(int epi, bool a4, bool w4, const GemmProblem& P) {
+  if (P.N <= 0 || P.K <= 0 || P.a_rows < 0 || P.groups < 1) return MOE_ERR_INVALID_ARG;
+  if (P.K % 64 != 0 || P.N % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!P.A || !P.W || !P.C) return MOE_ERR_INVALID_ARG;
+  if (!aligned(P.A, 16) || !aligned(P.W, 16) || !aligned(P.C, 16)) return MOE_ERR_INVALID_ARG;
+  if (a4 && (!P.A_sf || !P.A_g || !aligned(P.A_sf, 4))) return MOE_ERR_INVALID_ARG;
+  if (w4 && (!P.W_sf || !P.W_g || !aligned(P.W_sf, 4))) return MOE_ERR_INVALID_ARG;
+  if (epi == MOE_EPI_SWIGLU_NVFP4 && (!P.C_sf || !P.c_g || !aligned(P.C_sf, 2))) return MOE_ERR_INVALID_ARG;
+  const long long w_rows = static_cast<long long>(P.groups) * ((epi == MOE_EPI_STORE_BF16) ? P.N : 2 * P.N);
+  if (w_rows >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// Launches one persistent grouped GEMM over the routed problem (G groups,
+// device offsets) plus, when `sh` is non-null, the shared-expert problem as
+// one more group of `shared_rows` rows.
+int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed, const int32_t* offsets, int G,
+                        const GemmProblem* sh, int shared_rows, cudaStream_t s) {
+  const bool a4 = a_fmt == MOE_FMT_NVFP4, w4 = w_fmt == MOE_FMT_NVFP4;
+  if (G < 1 || G > gg::MAX_G - 1 || !offsets) return MOE_ERR_INVALID_ARG;
+  if (epi < MOE_EPI_STORE_BF16 || epi > MOE_EPI_SWIGLU_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (a4 && !w4) return MOE_ERR_UNSUPPORTED;
+  if (epi == MOE_EPI_SWIGLU_NVFP4 && !(a4 && w4)) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_problem(epi, a4, w4, routed));
+  if (sh) MOE_TRY(check_problem(epi, a4, w4, *sh));
+  // routed rows are T*k >= T shared rows, so an empty routed problem means
+  // there is nothing to do
+  if (routed.a_rows == 0) return MOE_OK;
+  const bool have_shared = sh != nullptr && shared_rows > 0;
+  gg::Params prm;
+  memset(&prm, 0, sizeof(prm));
+  MOE_TRY(fill_prob(prm, 0, epi, a4, w4, routed));
+  prm.offsets = offsets;
+  prm.G = G;
+  prm.shared_rows = -1;
+  if (have_shared) {
+    MOE_TRY(fill_prob(prm, 1, epi, a4, w4, *sh));
+    prm.shared_rows = shared_rows;
+  }
+  prm.err = device_error_word();
+  if (!prm.err) return MOE_ERR_CUDA;
+  prm.timeout_ns = wait_timeout_ns();
+  if (!a4 && !w4) {
+    if (epi == MOE_EPI_STORE_BF16) return launch_impl<MOE_EPI_STORE_BF16, false, false>(prm, s);
+    if (epi == MOE_EPI_SWIGLU_BF16) return launch_impl<MOE_EPI_SWIGLU_BF16, false, false>(prm, s);
+  } else if (!a4 && w4) {
+    if (epi == MOE_EPI_STORE_BF16) return launch_impl<MOE_EPI_STORE_BF16, false, true>(prm, s);
+    if (epi == MOE_EPI_SWIGLU_BF16) return launch_impl<MOE_EPI_SWIGLU_BF16, false, true>(prm, s);
+  } else {
+    if (epi == MOE_EPI_STORE_BF16) return launch_impl<MOE_EPI_STORE_BF16, true, true>(prm, s);
+    if (epi == MOE_EPI_SWIGLU_BF16) return launch_impl<MOE_EPI_SWIGLU_BF16, true, true>(prm, s);
+    if (epi == MOE_EPI_SWIGLU_NVFP4) return launch_impl<MOE_EPI_SWIGLU_NVFP4, true, true>(prm, s);
+  }
+  return MOE_ERR_UNSUPPORTED;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue, int G, const int32_t* offsets, int M_total, int N,
+                                int K, const void* A, const uint8_t* A_sf, const float* A_g, const void* W,
+                                const uint8_t* W_sf, const float* W_g, void* C, uint8_t* C_sf, const float* c_g,
+                                void* stream) {
+  if (M_total < 0) return MOE_ERR_INVALID_ARG;
+  if (M_total == 0) return MOE_OK;
+  GemmProblem P{A, A_sf, A_g, M_total, W, W_sf, W_g, G, C, C_sf, c_g, N, K};
+  return grouped_gemm_launch(epilogue, a_fmt, w_fmt, P, offsets, G, nullptr, 0, static_cast<cudaStream_t>(stream));
+}

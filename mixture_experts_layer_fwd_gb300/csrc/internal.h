@@ -1,0 +1,40 @@
+// Internal launchers shared between the translation units of the library.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+size_t permute_ws_bytes(int T, int k, int E);
+int permute_launch(const int32_t* idx, int T, int k, int E, const void* x_rows, int row_bytes, const uint8_t* x_sf,
+                   int sf_row_bytes, int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
+                   void* xp_rows, uint8_t* xp_sf, void* ws, size_t ws_bytes, cudaStream_t s);
+
+size_t quant_ws_bytes(int groups);
+int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float* g_in, uint8_t* codes, uint8_t* sf,
+                 float* g_out, void* ws, size_t ws_bytes, cudaStream_t s);
+
+int combine_launch(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, int T, int k, int H,
+                   uint16_t* out, cudaStream_t s);
+
+// One problem set of the grouped GEMM: all routed groups (rows given by
+// device offsets), or the shared expert as a single group over all tokens.
+struct GemmProblem {
+  const void* A;       // bf16 [a_rows, K] or packed E2M1 [a_rows, K/2]
+  const uint8_t* A_sf; // [a_rows, K/16] E4M3 (NVFP4 A)
+  const float* A_g;    // device scalar (NVFP4 A)
+  int a_rows;
+  const void* W;       // bf16 [groups * Wn, K] or packed E2M1 [groups * Wn, K/2]
+  const uint8_t* W_sf; // [groups * Wn, K/16] (NVFP4 W)
+  const float* W_g;    // [groups] (NVFP4 W)
+  int groups;
+  void* C;             // bf16 [a_rows, N] or packed E2M1 [a_rows, N/2]
+  uint8_t* C_sf;       // [a_rows, N/16] (NVFP4 C)
+  const float* c_g;    // device scalar (NVFP4 C)
+  int N, K;
+};
+
+int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed, const int32_t* offsets, int G,
+                        const GemmProblem* sh, int shared_rows, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,82 @@
+// NVFP4 helpers of the CUDA path: E4M3 scale encode/decode, E2M1 code
+// selection, and the 16-element block quantiser shared by the activation
+// quantiser and the NVFP4 SwiGLU epilogue of the grouped GEMM.
+//
+// Format ("Driving vLLM WideEP and Large-Scale Serving Toward Maturity on
+// Blackwell (Part I)", sections "NVFP4 GEMM for MoE and O-proj" and "NVFP4
+// MoE dispatch"): packed E2M1 codes, one E4M3 scale per 16 elements, one fp32
+// global scale g.  Recipe (IEEE fp32, round to nearest even):
+//   s = E4M3_satfinite(amax16 / (6 g)),  q_i = E2M1_satfinite(x_i / (e4m3(s) g))
+// with magnitude 0 when e4m3(s) == 0 and the code's sign bit = sign of x_i.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// fp32 -> E4M3 byte: round to nearest even, saturate to the largest finite
+// value (448).  Uses the hardware conversion.
+DEVINL uint32_t e4m3_encode_satfinite(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v), "f"(v));
+  return static_cast<uint32_t>(r) & 0xFFu;
+}
+
+// E4M3 byte -> fp32 (exact).  code (e<<3)|m: e == 0 -> m * 2^-9, else
+// (8 + m) * 2^(e - 10); bit 7 is the sign.
+DEVINL float e4m3_decode(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
+  return (b & 0x80u) ? -v : v;
+}
+
+// Magnitude code of a non-negative ratio: nearest of {0,.5,1,1.5,2,3,4,6},
+// ties to the even code, saturating at 6.  The decision points are the
+// midpoints between neighbours; at a midpoint the even code wins, which makes
+// the comparison strict (>) where the lower neighbour's code is even and
+// inclusive (>=) where it is odd.
+DEVINL uint32_t e2m1_magnitude(float a) {
+  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
+         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
+         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) + static_cast<uint32_t>(a > 5.0f);
+}
+
+// Quantise 16 fp32 values with global scale g.  Returns the E4M3 scale byte;
+// codes[0] holds elements 0..7 (element 2j in the low nibble of byte j),
+// codes[1] elements 8..15.
+DEVINL uint32_t nvfp4_quantize16(const float (&v)[16], float g, uint32_t (&codes)[2]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint32_t s = e4m3_encode_satfinite(__fdiv_rn(amax, __fmul_rn(6.0f, g)));
+  const float denom = __fmul_rn(e4m3_decode(s), g);
+  codes[0] = codes[1] = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint32_t mag = 0u;
+    if (denom != 0.0f) mag = e2m1_magnitude(fabsf(__fdiv_rn(v[i], denom)));
+    const uint32_t code = mag | ((__float_as_uint(v[i]) >> 31) << 3);
+    codes[i >> 3] |= code << (4 * (i & 7));
+  }
+  return s;
+}
+
+// bf16 bit pattern of each E2M1 code (sign in bit 3).
+DEVINL uint32_t e2m1_to_bf16_bits(uint32_t code) {
+  // magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+  const uint32_t mag = code & 7u;
+  uint32_t bits = 0u;
+  switch (mag) {
+    case 0: bits = 0x0000u; break;
+    case 1: bits = 0x3F00u; break;
+    case 2: bits = 0x3F80u; break;
+    case 3: bits = 0x3FC0u; break;
+    case 4: bits = 0x4000u; break;
+    case 5: bits = 0x4040u; break;
+    case 6: bits = 0x4080u; break;
+    default: bits = 0x40C0u; break;
+  }
+  return bits | ((code & 8u) << 12);
+}
+
+}  // namespace moe

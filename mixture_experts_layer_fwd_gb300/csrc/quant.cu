@@ -1,0 +1,121 @@
+// NVFP4 quantiser of bf16 matrices (activations before dispatch: "Driving
+// vLLM WideEP and Large-Scale Serving Toward Maturity on Blackwell (Part I)",
+// section "NVFP4 MoE dispatch"; the abs-max over 16 elements: "CuTeDSL at
+// Perplexity", Blackwell support).  Also used once per layer to turn bf16
+// master weights into NVFP4 weights (one global scale per expert).
+//
+// Two passes over x, both HBM-bound:
+//   amax  : grid-stride 16-byte loads, block max, atomicMax of the fp32 bit
+//           pattern (valid ordering for non-negative floats) into workspace
+//   quant : one thread per 16-element block: two 16-byte loads, scale byte,
+//           eight code bytes (one 8-byte store), coalesced across the warp
+#include "internal.h"
+#include "nvfp4.cuh"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, long long group_elems,
+                                                   unsigned int* __restrict__ amax_bits) {
+  const int g = blockIdx.y;
+  const uint4* p = reinterpret_cast<const uint4*>(x + static_cast<size_t>(g) * group_elems);
+  const long long nvec = group_elems / 8;
+  float m = 0.0f;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nvec;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(p + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+    atomicMax(amax_bits + g, __float_as_uint(m));
+  }
+}
+
+__global__ void __launch_bounds__(256) quant_kernel(const uint16_t* __restrict__ x, long long nblocks,
+                                                    long long blocks_per_group, const float* __restrict__ g_in,
+                                                    const unsigned int* __restrict__ amax_bits,
+                                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                    float* __restrict__ g_out) {
+  const long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (b >= nblocks) return;
+  const int grp = static_cast<int>(b / blocks_per_group);
+  float g;
+  if (g_in != nullptr) {
+    g = __ldg(g_in + grp);
+  } else {
+    const float amax = __uint_as_float(__ldg(amax_bits + grp));
+    g = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
+  }
+  if (b % blocks_per_group == 0) g_out[grp] = g;
+  const uint4* p = reinterpret_cast<const uint4*>(x + b * 16);
+  const uint4 lo = __ldg(p), hi = __ldg(p + 1);
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  uint32_t c[2];
+  const uint32_t s = nvfp4_quantize16(v, g, c);
+  reinterpret_cast<uint2*>(codes)[b] = make_uint2(c[0], c[1]);
+  sf[b] = static_cast<uint8_t>(s);
+}
+
+size_t quant_ws_bytes(int groups) { return round_up(static_cast<size_t>(groups) * sizeof(unsigned int), 256); }
+
+int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float* g_in, uint8_t* codes, uint8_t* sf,
+                 float* g_out, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const long long group_elems = static_cast<long long>(rows) * cols;
+  if (group_elems == 0 || groups == 0) return MOE_OK;
+  unsigned int* amax = static_cast<unsigned int*>(ws);
+  if (g_in == nullptr) {
+    if (ws_bytes < quant_ws_bytes(groups) || ws == nullptr) return MOE_ERR_WORKSPACE;
+    cudaError_t e = cudaMemsetAsync(amax, 0, static_cast<size_t>(groups) * sizeof(unsigned int), s);
+    if (e != cudaSuccess) {
+      set_cuda_error(e);
+      return MOE_ERR_CUDA;
+    }
+    const long long nvec = group_elems / 8;
+    int bx = static_cast<int>(std::min<long long>((nvec + 255) / 256, 4LL * num_sms() / std::max(1, groups) + 1));
+    bx = std::max(bx, 1);
+    dim3 grid(bx, groups);
+    amax_kernel<<<grid, 256, 0, s>>>(x, group_elems, amax);
+  }
+  const long long nblocks = group_elems / 16 * groups;
+  const long long nthreadblocks = (nblocks + 255) / 256;
+  quant_kernel<<<static_cast<unsigned int>(nthreadblocks), 256, 0, s>>>(x, nblocks, group_elems / 16, g_in, amax,
+                                                                         codes, sf, g_out);
+  return check_launch();
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_quant_nvfp4_workspace_size(int groups) {
+  if (groups < 1) return 0;
+  return quant_ws_bytes(groups);
+}
+
+extern "C" int moe_quant_nvfp4(const uint16_t* x, int groups, int rows, int cols, const float* g_in, uint8_t* codes,
+                               uint8_t* sf, float* g_out, void* ws, size_t ws_bytes, void* stream) {
+  if (groups < 1 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(rows) * cols == 0) return MOE_OK;
+  if (!x || !codes || !sf || !g_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(g_out, 4)) return MOE_ERR_INVALID_ARG;
+  if (g_in == nullptr && (ws == nullptr || ws_bytes < quant_ws_bytes(groups))) return MOE_ERR_WORKSPACE;
+  if (ws != nullptr && !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  return quant_launch(x, groups, rows, cols, g_in, codes, sf, g_out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,101 @@
+"""A ready-to-call MoE layer: owns the weights in the kernels' formats, the
+workspace, and the C struct that describes them to moe_forward.
+
+Weight preparation for the NVFP4 formats runs the library's own quantiser
+(moe_quant_nvfp4, one global scale per expert and projection).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import api
+from ._lib import MOE_FMT_BF16, MOE_FMT_NVFP4, MoeLayerC
+
+_FMT = {"bf16": MOE_FMT_BF16, "nvfp4": MOE_FMT_NVFP4}
+
+
+@dataclass
+class NVFP4Tensor:
+    codes: torch.Tensor  # uint8 [..., cols/2]
+    sf: torch.Tensor     # uint8 [..., cols/16]
+    g: torch.Tensor      # fp32 [groups]
+
+
+def quantize_weights(w: torch.Tensor) -> NVFP4Tensor:
+    """bf16 [groups, rows, cols] (or [rows, cols]) -> NVFP4 with one global
+    scale per group."""
+    codes, sf, g = api.moe_quant_nvfp4(w.contiguous())
+    return NVFP4Tensor(codes, sf, g)
+
+
+class MoELayer:
+    def __init__(self, H: int, E: int, k: int, I: int, I_s: int, w13: torch.Tensor, w2: torch.Tensor,
+                 ws13: Optional[torch.Tensor] = None, ws2: Optional[torch.Tensor] = None,
+                 w_fmt: str = "bf16", act_fmt: str = "bf16", g_h: float = 0.0, g_hs: Optional[float] = None):
+        """w13 bf16 [E, 2I, H], w2 bf16 [E, H, I], ws13 bf16 [2I_s, H], ws2 bf16
+        [H, I_s] on one CUDA device.  With w_fmt='nvfp4' they are quantised
+        here; act_fmt='nvfp4' also needs the static global scale g_h of the
+        SwiGLU output (g_hs for the shared expert, default g_h)."""
+        self.H, self.E, self.k, self.I, self.I_s = H, E, k, I, I_s
+        self.w_fmt, self.act_fmt = w_fmt, act_fmt
+        self.device = w13.device
+        self._keep = []
+        c = MoeLayerC()
+        c.H, c.E, c.k, c.I, c.I_s = H, E, k, I, I_s
+        c.w_fmt, c.act_fmt = _FMT[w_fmt], _FMT[act_fmt]
+        if w_fmt == "bf16":
+            self.w13, self.w2 = w13.contiguous(), w2.contiguous()
+            c.w13, c.w2 = self.w13.data_ptr(), self.w2.data_ptr()
+            self._keep += [self.w13, self.w2]
+            if I_s:
+                self.ws13, self.ws2 = ws13.contiguous(), ws2.contiguous()
+                c.ws13, c.ws2 = self.ws13.data_ptr(), self.ws2.data_ptr()
+                self._keep += [self.ws13, self.ws2]
+        else:
+            self.w13 = quantize_weights(w13)
+            self.w2 = quantize_weights(w2)
+            c.w13, c.w13_sf, c.w13_g = (t.data_ptr() for t in (self.w13.codes, self.w13.sf, self.w13.g))
+            c.w2, c.w2_sf, c.w2_g = (t.data_ptr() for t in (self.w2.codes, self.w2.sf, self.w2.g))
+            self._keep += [self.w13, self.w2]
+            if I_s:
+                self.ws13 = quantize_weights(ws13)
+                self.ws2 = quantize_weights(ws2)
+                c.ws13, c.ws13_sf, c.ws13_g = (t.data_ptr() for t in (self.ws13.codes, self.ws13.sf, self.ws13.g))
+                c.ws2, c.ws2_sf, c.ws2_g = (t.data_ptr() for t in (self.ws2.codes, self.ws2.sf, self.ws2.g))
+                self._keep += [self.ws13, self.ws2]
+        if act_fmt == "nvfp4":
+            self.g_h = torch.tensor([g_h], dtype=torch.float32, device=self.device)
+            self.g_hs = torch.tensor([g_h if g_hs is None else g_hs], dtype=torch.float32, device=self.device)
+            c.g_h, c.g_hs = self.g_h.data_ptr(), self.g_hs.data_ptr()
+        self.c = c
+        self._ws = None
+
+    @classmethod
+    def from_config(cls, cfg, weights) -> "MoELayer":
+        """From a synth.LayerConfig and synth.MasterWeights."""
+        return cls(cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_s, weights.w13, weights.w2, weights.ws13, weights.ws2,
+                   cfg.w_fmt, cfg.act_fmt, cfg.g_h)
+
+    def workspace_size(self, T: int) -> int:
+        n = api.moe_forward_workspace_size(self.c, T)
+        if n == 0 and T > 0:
+            raise ValueError("layer description rejected by moe_forward_workspace_size")
+        return n
+
+    def workspace(self, T: int) -> torch.Tensor:
+        n = self.workspace_size(T)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        return api.moe_forward(self.c, x, logits, out, self.workspace(T), stream)
+
+    __call__ = forward

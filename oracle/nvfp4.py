@@ -31,9 +31,10 @@ The sign bit of q always carries the sign of x (so -0.0 and tiny negatives
 encode as 0x8).  Two codes pack into one byte: element 2j in the low nibble,
 element 2j+1 in the high nibble.  Scales are raw E4M3 bytes, row-major.
 
-Everything here is written from those definitions: the encoders find the
+Everything here is written from those definitions: the E4M3 encoder finds the
 nearest representable value by comparing distances in fp64 (exact for fp32
-inputs) and break ties towards the even code.
+inputs); the E2M1 encoder compares against the midpoints of its 8-value grid;
+both break ties towards the even code.
 """
 from __future__ import annotations
 
@@ -104,22 +105,25 @@ def e2m1_decode(q: np.ndarray) -> np.ndarray:
     return np.where(q & 8, -mag, mag).astype(F32)
 
 
+# Rounding to the nearest grid magnitude, ties to the even code, written
+# through the midpoints between neighbouring magnitudes: a value moves past a
+# midpoint when it lies strictly above it, or exactly on it when the upper
+# neighbour has the even code.  Values above the largest midpoint saturate to
+# the largest magnitude.
+E2M1_MIDPOINTS = ((E2M1_GRID[1:] + E2M1_GRID[:-1]) / 2).astype(np.float32)
+E2M1_TIE_GOES_UP = (np.arange(1, 8) % 2) == 0
+
+
 def e2m1_encode(v: np.ndarray) -> np.ndarray:
     """fp32 -> 4-bit code, round to nearest grid magnitude, ties to the even
     code, saturating to 6.  Sign bit = sign of the input (also for zeros)."""
     v = np.asarray(v, dtype=F32)
-    a = np.abs(v.astype(np.float64))
-    grid = E2M1_GRID
-    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, len(grid) - 1)
-    lo = np.clip(hi - 1, 0, len(grid) - 1)
-    d_lo = np.abs(a - grid[lo])
-    d_hi = np.abs(a - grid[hi])
-    code = np.where(d_lo < d_hi, lo, hi)
-    tie = d_lo == d_hi
-    code = np.where(tie, np.where(lo % 2 == 0, lo, hi), code)
-    code = np.where(a >= grid[-1], len(grid) - 1, code)
+    a = np.abs(v)
+    mag = np.zeros(v.shape, dtype=np.uint8)
+    for mid, up in zip(E2M1_MIDPOINTS, E2M1_TIE_GOES_UP):
+        mag += (a >= mid) if up else (a > mid)
     sign = np.signbit(v).astype(np.uint8) << 3
-    return (code.astype(np.uint8) | sign).astype(np.uint8)
+    return (mag | sign).astype(np.uint8)
 
 
 def global_scale(x: np.ndarray) -> np.float32:

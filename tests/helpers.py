@@ -1,0 +1,77 @@
+"""Shared helpers of the GPU parity tests: oracle-side weight decoding and
+the layer runner.  Every expected value here is computed by oracle/ from the
+seeded inputs of synth/; nothing is read back from the CUDA path except the
+results under test."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+from oracle import nvfp4
+
+F32 = np.float32
+
+
+def require_gpu():
+    import pytest
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as g
+    g.build()
+
+
+def to_np_f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").to(torch.float32).numpy()
+
+
+class OracleWeights:
+    """Oracle view of the master weights: fp64 dequantised per expert, with
+    the oracle's own NVFP4 quantiser on the NVFP4 workloads (one global scale
+    per expert and projection, like the CUDA path's weight preparation)."""
+
+    def __init__(self, cfg: synth.LayerConfig, master: synth.MasterWeights):
+        self.cfg, self.m = cfg, master
+        self.cache = {}
+
+    def _decode(self, w: torch.Tensor):
+        a = to_np_f32(w)
+        if self.cfg.w_fmt == "bf16":
+            return a.astype(np.float64), None
+        q, s, g = nvfp4.quantize(a)
+        return nvfp4.dequantize(q, s, g), (q, s, g)
+
+    def expert(self, e: int) -> oracle.ExpertWeights:
+        if e not in self.cache:
+            w13, _ = self._decode(self.m.w13[e])
+            w2, _ = self._decode(self.m.w2[e])
+            self.cache[e] = oracle.ExpertWeights(w13, w2)
+        return self.cache[e]
+
+    def expert_codes(self, e: int):
+        """Oracle NVFP4 encoding of expert e: ((q13, s13, g13), (q2, s2, g2))."""
+        return self._decode(self.m.w13[e])[1], self._decode(self.m.w2[e])[1]
+
+    def shared(self):
+        if self.cfg.I_s == 0:
+            return None
+        if "shared" not in self.cache:
+            w13, _ = self._decode(self.m.ws13)
+            w2, _ = self._decode(self.m.ws2)
+            self.cache["shared"] = oracle.ExpertWeights(w13, w2)
+        return self.cache["shared"]
+
+
+def oracle_layer(cfg: synth.LayerConfig, acts: synth.Activations, ow: OracleWeights, tokens=None):
+    """Oracle output (fp64) for the given tokens, plus idx / w / perm over all T."""
+    x = to_np_f32(acts.x)
+    if cfg.act_fmt == "nvfp4":
+        q, s, g = nvfp4.quantize(x)  # one global scale over the whole input
+        x_deq = nvfp4.dequantize(q, s, g)
+        gh = F32(cfg.g_h)
+    else:
+        x_deq = x.astype(np.float64)
+        gh = None
+    return oracle.forward(x_deq, acts.logits.numpy(), cfg.k, cfg.E, ow.expert, ow.shared(), tokens=tokens,
+                          h_quant_g=gh, hs_quant_g=gh)

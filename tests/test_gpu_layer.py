@@ -1,0 +1,143 @@
+"""Layer parity: moe_forward (through the C ABI) against the fp64 oracle.
+
+Tolerance (relative Frobenius error of the bf16 output): 5e-3 on the bf16
+weight path, 1e-2 on the NVFP4 paths.  Small shapes are compared on every
+token; the full-size workloads on a seeded token subsample (each output row
+depends only on its own token and the global activation scale, so the
+oracle evaluates those rows exactly)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import nvfp4
+from tests.helpers import OracleWeights, oracle_layer, require_gpu, to_np_f32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _tol(cfg):
+    return 5e-3 if cfg.w_fmt == "bf16" else 1e-2
+
+
+def _run(cfg, T, seed=0, tokens=None, weights=None):
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
+    acts = synth.make_activations(cfg, T, seed=seed)
+    w = weights or synth.make_weights(cfg, seed=seed, device=DEV)
+    layer = MoELayer.from_config(cfg, w)
+    out = layer(acts.x.to(DEV), acts.logits.to(DEV))
+    assert moe_sync_status() == 0
+    got = to_np_f32(out)
+    assert np.isfinite(got).all()
+    ref, *_ = oracle_layer(cfg, acts, OracleWeights(cfg, w), tokens=tokens)
+    sel = got if tokens is None else got[tokens]
+    return oracle.rel_frobenius(sel, ref), layer, w
+
+
+SMALL = {
+    "qwen3-235b": synth.small_variant(synth.QWEN3_235B, H=512, E=16, k=4, I=256),
+    "qwen35-397b": synth.small_variant(synth.QWEN35_397B, H=512, E=32, k=5, I=128, I_s=192),
+    "deepseek-v3": synth.small_variant(synth.DEEPSEEK_V3, H=768, E=16, k=4, I=256, I_s=320),
+}
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_layer_all_tokens(seed):
+    cfg = synth.TINY
+    err, *_ = _run(cfg, 64, seed=seed)
+    assert err <= _tol(cfg), err
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("T", [1, 37, 300])
+def test_small_layers_all_tokens(name, T):
+    cfg = SMALL[name]
+    err, *_ = _run(cfg, T, seed=T)
+    assert err <= _tol(cfg), err
+
+
+def test_zero_tokens_is_noop():
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
+    cfg = synth.TINY
+    layer = MoELayer.from_config(cfg, synth.make_weights(cfg, 0, DEV))
+    out = torch.full((0, cfg.H), 7, dtype=torch.bfloat16, device=DEV)
+    layer(torch.empty(0, cfg.H, dtype=torch.bfloat16, device=DEV), torch.empty(0, cfg.E, device=DEV), out=out)
+    assert moe_sync_status() == 0
+
+
+def test_k_equals_E_and_single_expert():
+    for cfg in (synth.small_variant(synth.TINY, H=256, E=4, k=4, I=128),
+                synth.small_variant(synth.TINY, H=256, E=1, k=1, I=192)):
+        err, *_ = _run(cfg, 50, seed=4)
+        assert err <= 5e-3, (cfg, err)
+
+
+def test_hot_experts_leave_others_empty():
+    cfg = synth.small_variant(synth.DEEPSEEK_V3, H=512, E=64, k=4, I=128, I_s=128)
+    from dataclasses import replace
+    cfg = replace(cfg, zipf=2.0)
+    err, *_ = _run(cfg, 200, seed=6)
+    assert err <= 1e-2, err
+
+
+def test_decode_one_token_per_expert():
+    """All experts active with a single token each ("Hosting Qwen on
+    Blackwell", section "MoE GEMM" microbenchmarks), on small shapes."""
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
+    cfg = SMALL["qwen3-235b"]
+    T, logits = synth.forced_one_token_per_expert_logits(cfg)
+    acts = synth.make_activations(cfg, T, seed=1)
+    acts = synth.Activations(acts.x, logits)
+    w = synth.make_weights(cfg, 1, DEV)
+    out = MoELayer.from_config(cfg, w)(acts.x.to(DEV), acts.logits.to(DEV))
+    assert moe_sync_status() == 0
+    ref, idx, *_ = oracle_layer(cfg, acts, OracleWeights(cfg, w))
+    assert sorted(idx.reshape(-1).tolist()) == list(range(cfg.E))
+    assert oracle.rel_frobenius(to_np_f32(out), ref) <= 5e-3
+
+
+def test_nvfp4_weight_codes_match_oracle():
+    """The layer's NVFP4 weight preparation (library quantiser) is bit-exact
+    with the oracle's encoding of the same bf16 master weights."""
+    from mixture_experts_layer_fwd_gb300 import MoELayer
+    cfg = SMALL["qwen35-397b"]
+    w = synth.make_weights(cfg, 0, DEV)
+    layer = MoELayer.from_config(cfg, w)
+    ow = OracleWeights(cfg, w)
+    for e in (0, 7, cfg.E - 1):
+        (q13, s13, g13), (q2, s2, g2) = ow.expert_codes(e)
+        assert np.array_equal(layer.w13.codes[e].cpu().numpy(), q13)
+        assert np.array_equal(layer.w13.sf[e].cpu().numpy(), s13)
+        assert layer.w13.g[e].item() == g13
+        assert np.array_equal(layer.w2.codes[e].cpu().numpy(), q2)
+        assert np.array_equal(layer.w2.sf[e].cpu().numpy(), s2)
+
+
+# ------------------------------------------------------- full-size workloads
+FULL = [("qwen3-235b", 256, 24), ("qwen3-235b", 8192, 12), ("qwen35-397b", 64, 8), ("qwen35-397b", 512, 6),
+        ("qwen35-397b", 4096, 6), ("deepseek-v3", 256, 3), ("deepseek-v3", 16384, 3)]
+
+
+@pytest.mark.parametrize("name,T,n", FULL)
+def test_full_size_sampled_tokens(name, T, n):
+    cfg = synth.CONFIGS[name]
+    toks = synth.sample_tokens(T, n, seed=T)
+    err, *_ = _run(cfg, T, seed=0, tokens=toks)
+    assert err <= _tol(cfg), err
+
+
+@pytest.mark.parametrize("w_fmt,zipf,T", [("bf16", 2.0, 1), ("bf16", 0.0, 4096), ("nvfp4", 2.0, 65536),
+                                          ("nvfp4", 0.0, 2)])
+def test_sweep_points(w_fmt, zipf, T):
+    """Size / imbalance sweep on the DeepSeek-V3 shapes (sampled tokens)."""
+    cfg = synth.sweep_config(w_fmt, zipf)
+    toks = synth.sample_tokens(T, 2, seed=T)
+    err, *_ = _run(cfg, T, seed=0, tokens=toks)
+    assert err <= _tol(cfg), err

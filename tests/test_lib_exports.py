@@ -1,0 +1,93 @@
+"""The C-ABI library builds, loads without a GPU, and exports every function
+declared in include/*.h; host-side argument checks reject bad input before
+anything touches a device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+\**\s*(moe_[a-z0-9_]+)\s*\(",
+                             src, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from mixture_experts_layer_fwd_gb300 import _lib
+    return _lib.load()
+
+
+def test_header_declares_the_six_stage_calls():
+    names = _declared_functions()
+    for n in ["moe_route", "moe_permute", "moe_quant_nvfp4", "moe_grouped_gemm", "moe_combine", "moe_forward"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 10
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_symbol():
+    from mixture_experts_layer_fwd_gb300 import _lib
+    assert set(_declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.moe_version() == 100
+    assert lib.moe_status_string(0) == b"MOE_OK"
+    assert lib.moe_status_string(5) == b"MOE_ERR_TIMEOUT"
+
+
+def test_host_argument_checks_without_gpu(lib):
+    from mixture_experts_layer_fwd_gb300 import _lib as L
+    # k > E, E too large, negative T: rejected on the host
+    assert lib.moe_route(None, 4, 8, 9, None, None, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(None, 4, 2048, 2, None, None, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(None, -1, 8, 2, None, None, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(None, 4, 8, 2, None, None, None) == L.MOE_ERR_INVALID_ARG
+    # T == 0 is a no-op
+    assert lib.moe_route(None, 0, 8, 2, None, None, None) == L.MOE_OK
+    assert lib.moe_combine(None, None, None, None, 0, 2, 256, None, None) == L.MOE_OK
+    assert lib.moe_combine(None, None, None, None, 4, 2, 250, None, None) == L.MOE_ERR_UNSUPPORTED
+    # quantiser: cols not a multiple of 16
+    assert lib.moe_quant_nvfp4(None, 1, 4, 24, None, None, None, None, None, 0, None) == L.MOE_ERR_UNSUPPORTED
+    # grouped GEMM: K not a multiple of 64
+    assert lib.moe_grouped_gemm(0, 0, 0, 4, ctypes.c_void_p(256), 128, 256, 96, ctypes.c_void_p(256), None,
+                                None, ctypes.c_void_p(256), None, None, ctypes.c_void_p(256), None, None,
+                                None) == L.MOE_ERR_UNSUPPORTED
+    # permute workspace grows with the number of chunks
+    assert lib.moe_permute_workspace_size(0, 8, 128) == 0
+    assert lib.moe_permute_workspace_size(16384, 8, 256) > lib.moe_permute_workspace_size(256, 8, 256)
+
+
+def test_forward_layer_validation(lib):
+    from mixture_experts_layer_fwd_gb300 import _lib as L
+    c = L.MoeLayerC()
+    c.H, c.E, c.k, c.I, c.I_s = 4096, 128, 8, 1536, 0
+    c.w_fmt = c.act_fmt = L.MOE_FMT_BF16
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), 256) == 0  # no weights given
+    c.w13, c.w2 = 4096, 8192
+    n = lib.moe_forward_workspace_size(ctypes.byref(c), 256)
+    # Xp + Y dominate: 2 * T*k*H*2 bytes
+    assert n >= 2 * 256 * 8 * 4096 * 2
+    c.H = 4000
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), 256) == 0
+    c.H = 4096
+    c.act_fmt = L.MOE_FMT_NVFP4  # NVFP4 activations need NVFP4 weights
+    assert lib.moe_forward(ctypes.byref(c), None, None, 4, None, None, 0, None) == L.MOE_ERR_UNSUPPORTED

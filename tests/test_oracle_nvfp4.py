@@ -53,6 +53,28 @@ def test_e4m3_hand_table(golden_dir):
     assert not bad, bad
 
 
+def _e2m1_brute(v):
+    """Nearest grid magnitude by explicit distances in fp64, ties to the even
+    code, sign from the input."""
+    out = []
+    for x in np.asarray(v, F32).tolist():
+        a = abs(x)
+        d = [abs(a - g) for g in nvfp4.E2M1_GRID]
+        best = min(range(8), key=lambda c: (d[c], c % 2))
+        out.append(best | (8 if np.signbit(np.float32(x)) else 0))
+    return np.array(out, np.uint8)
+
+
+def test_e2m1_matches_distance_brute_force():
+    rng = np.random.default_rng(4)
+    grid = nvfp4.E2M1_GRID
+    mids = (grid[1:] + grid[:-1]) / 2
+    vals = np.concatenate([rng.uniform(-8, 8, 4000), rng.standard_normal(2000), mids, -mids, grid, -grid,
+                           np.nextafter(mids.astype(F32), np.float32(0)), np.nextafter(mids.astype(F32), np.float32(9))])
+    vals = vals.astype(F32)
+    assert np.array_equal(nvfp4.e2m1_encode(vals), _e2m1_brute(vals))
+
+
 def test_e2m1_grid_round_trips():
     codes = np.arange(16, dtype=np.uint8)
     vals = nvfp4.e2m1_decode(codes)
