@@ -146,6 +146,27 @@ int moe_permute(const int32_t* idx, int T, int k, int E,
                 void* xp_rows, uint8_t* xp_sf,
                 void* ws, size_t ws_bytes, void* stream);
 
+/* moe_permute without a caller workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory at
+ * dispatch time -- runtimes that hand out a fixed set of buffers at start-up
+ * and forbid allocation on the per-step path (cudaMalloc may synchronise the
+ * device and has unbounded latency), embedders whose own allocator owns all
+ * device memory, plugins that only receive their inputs and outputs.
+ * Same arguments, results and checks as moe_permute, minus ws / ws_bytes.
+ * Its scratch is a 1 MiB array defined by the library in device memory
+ * (held on every device that loads the library until the process exits),
+ * which limits the size to ceil(T*k / 1024) * E <= 131072 (e.g. T*k <= 131072
+ * with E <= 1024); larger problems return MOE_ERR_UNSUPPORTED before any
+ * launch.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the array: calls that overlap on the GPU race on it, calls
+ * ordered on one stream do not.  No allocation of any kind is made. */
+int moe_permute_noalloc(const int32_t* idx, int T, int k, int E,
+                        const void* x_rows, int row_bytes,
+                        const uint8_t* x_sf, int sf_row_bytes,
+                        int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
+                        void* xp_rows, uint8_t* xp_sf, void* stream);
+
 /* ------------------------------------------------------------ quant_nvfp4
  * NVFP4 quantisation of bf16 matrices (activations before dispatch:
  * "Driving vLLM WideEP ... (Part I)", section "NVFP4 MoE dispatch"; abs-max

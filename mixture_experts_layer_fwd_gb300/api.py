@@ -100,6 +100,38 @@ def moe_permute(idx: torch.Tensor, E: int, x_rows: Optional[torch.Tensor] = None
     return dict(counts=counts, offsets=offsets, row_of=row_of, src_tok=src_tok, xp=xp, xp_sf=xp_sf)
 
 
+def moe_permute_noalloc(idx: torch.Tensor, E: int, x_rows: Optional[torch.Tensor] = None,
+                        x_sf: Optional[torch.Tensor] = None, out: Optional[dict] = None, stream=None):
+    """moe_permute for callers that cannot allocate device memory when they
+    dispatch: the library keeps the scratch in its own fixed device array
+    (size limit ceil(T*k/1024) * E <= 131072).  Pass preallocated outputs in
+    `out` (keys counts, offsets, row_of, src_tok, xp, xp_sf) to make the call
+    allocation-free end to end; missing outputs are allocated here."""
+    _dev(idx)
+    T, k = idx.shape
+    dev = idx.device
+    o = dict(out or {})
+    o.setdefault("counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("row_of", torch.empty(T, k, dtype=torch.int32, device=dev))
+    o.setdefault("src_tok", torch.empty(T * k, dtype=torch.int32, device=dev))
+    row_bytes = sf_bytes = 0
+    if x_rows is not None:
+        _dev(x_rows)
+        row_bytes = x_rows[0].numel() * x_rows.element_size() if T else 0
+        o.setdefault("xp", torch.empty((T * k,) + tuple(x_rows.shape[1:]), dtype=x_rows.dtype, device=dev))
+        if x_sf is not None:
+            _dev(x_sf)
+            sf_bytes = x_sf.shape[1]
+            o.setdefault("xp_sf", torch.empty(T * k, sf_bytes, dtype=torch.uint8, device=dev))
+    o.setdefault("xp", None)
+    o.setdefault("xp_sf", None)
+    check(load().moe_permute_noalloc(_ptr(idx), T, k, E, _ptr(x_rows), row_bytes, _ptr(x_sf), sf_bytes,
+                                     _ptr(o["counts"]), _ptr(o["offsets"]), _ptr(o["row_of"]), _ptr(o["src_tok"]),
+                                     _ptr(o["xp"]), _ptr(o["xp_sf"]), _stream(stream)), "moe_permute_noalloc")
+    return o
+
+
 def moe_quant_nvfp4(x: torch.Tensor, g_in: Optional[torch.Tensor] = None, stream=None):
     """x bf16 [rows, cols] or [groups, rows, cols] -> (codes uint8 [..., cols/2],
     sf uint8 [..., cols/16], g fp32 [groups])."""
