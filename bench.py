@@ -1,15 +1,18 @@
 """Benchmark of the MoE FFN layer forward on GB300.
 
-Workload: the Qwen3-235B-shaped layer (H=4096, 128 experts, top-8 softmax
-renormalised, expert intermediate 1536, SwiGLU, no shared expert, bf16
-weights and activations), T = 8192 tokens (prefill), seeded synthetic inputs
-(x ~ N(0,1), router bias from Zipf(1.1) ranks, weights ~ N(0, 0.02)).
+Default workload (the benchmark line): the Qwen3-235B-shaped layer (H=4096,
+128 experts, top-8 softmax renormalised, expert intermediate 1536, SwiGLU,
+no shared expert, bf16 weights and activations), T = 8192 tokens, seeded
+synthetic inputs (x ~ N(0,1), router bias from Zipf(1.1) ranks, weights
+~ N(0, 0.02)).  --config / --T / --zipf / --w-fmt select any other
+workload of synth/ (the NVFP4 layers, the DeepSeek-V3 sweep).
 
-One step = one moe_forward over the whole batch: route, permute, grouped
-GEMM gate/up + SwiGLU, grouped GEMM down, combine.  Inputs are resident in
-HBM; L2 is flushed (a 256 MB write) before every timed step, outside the
-step's events.  Each step records CUDA events at the stage boundaries
-(moe_forward_profiled), which gives the grouped-GEMM kernel time live.
+One step = one moe_forward over the whole batch: route, (NVFP4 activation
+quantisation), permute, grouped GEMM gate/up + SwiGLU, grouped GEMM down,
+combine.  Inputs are resident in HBM; L2 is flushed (a 256 MB write) before
+every timed step, outside the step's events.  Each step records CUDA events
+at the stage boundaries (moe_forward_profiled), which gives the
+grouped-GEMM kernel time live.
 
 Prints one JSON line.  --impl reference times the fp64 CPU oracle on the
 same workload (bounded token samples per step) instead.
@@ -21,6 +24,7 @@ GPU and the job value is the sum of tokens over the max per-rank time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -41,8 +45,18 @@ import synth  # noqa: E402
 CFG = synth.QWEN3_235B
 T_MAIN = 8192
 T_DECODE = 256
-METRIC = "MoE-layer tokens/s (Qwen3-235B-shaped bf16 layer, T=8192)"
 UNIT = "tokens/s"
+# nominal dense FP4 / bf16 tensor throughput ratio of GB300 (13.5 / 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0
+
+# Profiling case for ncu captures: same H, k, I and rows per expert as the
+# main workload (T*k/E = 512), 32 experts and T=2048 (1.2 GB of weights).
+SMALL_CFG = synth.small_variant(CFG, H=4096, E=32, k=8, I=1536, name="qwen3-235b-e32")
+T_SMALL = 2048
+
+
+def metric_name(cfg, T):
+    return f"MoE-layer tokens/s ({cfg.name} layer, {cfg.w_fmt} weights, {cfg.act_fmt} activations, T={T})"
 
 
 def peaks():
@@ -72,6 +86,7 @@ class ClockSampler:
                  "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            time.sleep(0.3)  # let the sampler start before the timed region
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -152,6 +167,78 @@ def max_over_ranks(v: float, world: int, device) -> float:
     return float(t.item())
 
 
+def workload(args):
+    if args.workload == "small":
+        return SMALL_CFG, T_SMALL
+    if args.config is None:
+        return CFG, (args.T or T_MAIN)
+    if args.config == "deepseek-v3-sweep":
+        cfg = synth.sweep_config(args.w_fmt or "nvfp4", args.zipf if args.zipf is not None else 1.1)
+    else:
+        cfg = synth.CONFIGS[args.config]
+        if args.zipf is not None:
+            cfg = dataclasses.replace(cfg, zipf=args.zipf)
+    T = args.T or max(cfg.Ts)
+    if args.experts:
+        # profiling variant: fewer experts, same tokens per expert (T*k/E)
+        T = max(1, T * args.experts // cfg.E)
+        cfg = dataclasses.replace(cfg, E=args.experts, name=f"{cfg.name}-e{args.experts}")
+    return cfg, T
+
+
+# ------------------------------------------------------------------ model
+def bytes_per_elem(fmt: str) -> float:
+    return 2.0 if fmt == "bf16" else 0.5625  # NVFP4: 4-bit code + one E4M3 byte per 16
+
+
+def gemm_work(cfg, T, active_experts):
+    """Algorithmic flops and DRAM bytes of the two grouped-GEMM launches of
+    one step: weights of the experts that received tokens (+ shared expert),
+    A read once, C written once."""
+    flops = cfg.flops_per_token() * T
+    wb = bytes_per_elem(cfg.w_fmt)
+    ab = bytes_per_elem(cfg.act_fmt)
+    Tk = T * cfg.k
+    weights = (active_experts * 3 * cfg.H * cfg.I + 3 * cfg.H * cfg.I_s) * wb
+    acts = (Tk * cfg.H + T * cfg.H * (1 if cfg.I_s else 0)) * ab      # GEMM1 A
+    acts += 2 * (Tk * cfg.I + T * cfg.I_s) * ab                       # h written, read back
+    acts += (Tk + (T if cfg.I_s else 0)) * cfg.H * 2                  # GEMM2 output (bf16)
+    return flops, weights + acts, weights
+
+
+def tensor_peak(cfg, p):
+    """Dense tensor peak of the MMA the path runs: bf16 (bf16 layers and the
+    NVFP4-weight / bf16-activation layer, whose MMA is bf16), or NVFP4 (both
+    operands NVFP4: block-scaled FP4 MMA) = measured bf16 x the nominal ratio."""
+    if cfg.w_fmt == "nvfp4" and cfg.act_fmt == "nvfp4":
+        return p["bf16_tflops"] * FP4_OVER_BF16, "nvfp4", f"bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16)"
+    return p["bf16_tflops"], "bf16", "bf16_tflops (burst)"
+
+
+def roofline(cfg, T, gemm_ms, active, traffic, src):
+    p, _ = peaks()
+    flops, nbytes, wbytes = gemm_work(cfg, T, active)
+    tpk, mma, how = tensor_peak(cfg, p)
+    t_tensor = flops / (tpk * 1e12)
+    t_hbm = nbytes / (p["hbm_gbs"] * 1e9)
+    sec = gemm_ms / 1e3
+    if t_tensor >= t_hbm:
+        ach = flops / sec / 1e12
+        r = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
+             "frac": round(ach / tpk, 4), "peak_source": f"{how} of {src} peaks",
+             "algorithmic": f"{flops / 2 / 1e9:.1f} GFLOP per launch ({cfg.flops_per_token() / 1e6:.1f} "
+                            f"MFLOP/token x {T} tokens / 2 launches)"}
+    else:
+        ach = nbytes / sec / 1e9
+        r = {"bound": "hbm", "achieved": round(ach, 1), "peak": p["hbm_gbs"], "unit": "GB/s",
+             "frac": round(ach / p["hbm_gbs"], 4), "peak_source": f"hbm_gbs of {src} peaks",
+             "algorithmic": f"{nbytes / 2 / 1e9:.3f} GB per launch ({wbytes / 1e9:.3f} GB of weights of "
+                            f"{active} active experts per step)"}
+    r.update({"traffic": traffic, "kernel": "grouped_gemm_kernel (2 launches/step)", "mma": mma,
+              "t_roof_ms": round(max(t_tensor, t_hbm) * 1e3, 4)})
+    return r
+
+
 # ------------------------------------------------------------------ oracle
 def oracle_tokens_per_s(cfg, acts, w_host, tokens):
     """Time the fp64 oracle (as it stands) on `tokens` of the workload."""
@@ -180,8 +267,8 @@ def cpu_threads() -> int:
 
 
 def run_reference(args):
-    """--impl reference: the CPU oracle on the same workload, K timed steps of
-    bounded token samples."""
+    """--impl reference: the CPU oracle on the bench workload, K timed steps
+    of bounded token samples."""
     world, rank, _ = dist_setup()
     if rank != 0:
         return
@@ -194,43 +281,29 @@ def run_reference(args):
     probe = synth.sample_tokens(T, 8, seed=1)
     _, t8 = oracle_tokens_per_s(cfg, acts, w_host, probe)
     budget = 180.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(512, 8 * budget / max(t8, 1e-3))))
-    rates, times = [], []
+    n = int(max(1, min(T, 8 * budget / max(t8, 1e-3))))
+    times = []
     for i in range(args.warmup + args.steps):
         toks = synth.sample_tokens(T, n, seed=100 + i)
-        r, dt = oracle_tokens_per_s(cfg, acts, w_host, toks)
+        _, dt = oracle_tokens_per_s(cfg, acts, w_host, toks)
         if i >= args.warmup:
-            rates.append(r)
             times.append(dt)
-    total_tok = n * args.steps
-    value = total_tok / sum(times)
-    cores = cpu_threads()
+    value = n * args.steps / sum(times)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"qwen3-235b moe layer bf16 weights, T={T} (oracle on {n}-token samples)",
+        "impl": "reference", "metric": metric_name(cfg, T), "value": round(value, 3), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} moe layer bf16 weights, T={T} (oracle on {n}-token samples)",
                    "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "T": T, "zipf": cfg.zipf},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                          "sample": f"{n} seeded tokens of the T={T} batch per step (rows are token-independent)"},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ GPU arm
-# Profiling case for ncu captures: same H, k, I and rows per expert as the
-# main workload (T*k/E = 512), 32 experts and T=2048 (1.2 GB of weights).
-SMALL_CFG = synth.small_variant(CFG, H=4096, E=32, k=8, I=1536, name="qwen3-235b-e32")
-T_SMALL = 2048
-
-
-def workload(args):
-    if args.workload == "small":
-        return SMALL_CFG, T_SMALL
-    return CFG, T_MAIN
-
-
 def run_gpu(args):
     from mixture_experts_layer_fwd_gb300 import MoELayer, api, moe_sync_status
     from mixture_experts_layer_fwd_gb300 import build as _build
@@ -240,30 +313,36 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     _build.build()
     cfg, T = workload(args)
+    is_main = args.workload == "main" and args.config is None and T == T_MAIN
     acts = synth.make_activations(cfg, T, seed=0)
     w = synth.make_weights(cfg, seed=0, device=str(dev))
     layer = MoELayer.from_config(cfg, w)
+    keep_master = rank == 0 and world == 1 and is_main and not args.no_cpu_baseline
+    if cfg.w_fmt == "nvfp4" or not keep_master:
+        w_host = (w.w13.cpu(), w.w2.cpu()) if keep_master else None
+        if cfg.w_fmt == "nvfp4":
+            del w  # the layer holds the NVFP4 weights; free the bf16 master
+            torch.cuda.empty_cache()
+    else:
+        w_host = None
     x = acts.x.to(dev)
     logits = acts.logits.to(dev)
     out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
     ws = layer.workspace(T)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
 
-    def step(evs):
-        api.moe_forward_profiled(layer.c, x, logits, out, ws, evs)
-
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    warm = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-    for ev in warm:
-        ev.record()  # creates the underlying CUDA events
-    for evs in evsets:
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
         for ev in evs:
-            ev.record()
+            ev.record()  # creates the underlying CUDA events
+        return evs
+
+    evsets = [new_events() for _ in range(args.steps)]
+    warm = new_events()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         flush.zero_()
-        step(warm)
+        api.moe_forward_profiled(layer.c, x, logits, out, ws, warm)
     torch.cuda.synchronize()
     if moe_sync_status() != 0:
         raise RuntimeError("device status not clean after warm-up")
@@ -274,7 +353,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
-        step(evsets[i])
+        api.moe_forward_profiled(layer.c, x, logits, out, ws, evsets[i])
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
@@ -286,20 +365,11 @@ def run_gpu(args):
     total_ms = max_over_ranks(float(sum(step_ms)), world, dev)
     value = world * T * args.steps / (total_ms / 1e3)
 
-    # grouped GEMM kernel: two launches per step (gate/up + SwiGLU, down)
-    flops = cfg.flops_per_token() * T
+    idx, _ = api.moe_route(logits, cfg.k)
+    active = int((torch.bincount(idx.reshape(-1).long(), minlength=cfg.E) > 0).sum())
     gemm_ms = float(np.mean(stage_ms[:, 3] + stage_ms[:, 4]))
-    p, src = peaks()
-    # the timed region is well under a second, so the burst figure applies
-    peak = p["bf16_tflops"]
-    achieved = flops / (gemm_ms / 1e3) / 1e12
-    traffic = gemm_traffic_per_launch() if args.workload == "main" else None
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "grouped_gemm_kernel (2 launches/step)",
-                "peak_source": f"bf16_tflops (burst) of {src} peaks",
-                "algorithmic": f"{flops / 2 / 1e9:.1f} GFLOP per launch ({cfg.flops_per_token() / 1e6:.1f} "
-                               f"MFLOP/token x {T} tokens / 2 launches)"}
+    _, src = peaks()
+    roof = roofline(cfg, T, gemm_ms, active, gemm_traffic_per_launch() if is_main else None, src)
 
     # e2e through the C ABI with host buffers (pinned), copies inside the timing
     xh = acts.x.pin_memory()
@@ -317,52 +387,49 @@ def run_gpu(args):
         api.moe_forward_host(layer.c, xh, lh, oh, xd, ld, out, ws)
         e2e_t.append(time.perf_counter() - t0)
     e2e_s = max_over_ranks(float(np.mean(e2e_t)), world, dev)
-    h2d = T * cfg.H * 2 + T * cfg.E * 4
-    d2h = T * cfg.H * 2
 
-    # decode-size point on the same weights (weight-streaming bound)
-    Td = T_DECODE
-    xd_ = x[:Td].contiguous()
-    ld_ = logits[:Td].contiguous()
-    od_ = out[:Td]
-    dec = []
-    evd = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-    for ev in evd:
-        ev.record()
-    for i in range(args.warmup + 10):
-        flush.zero_()
-        api.moe_forward_profiled(layer.c, xd_, ld_, od_, ws, evd)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            dec.append(evd[0].elapsed_time(evd[6]))
-    idx_d, _ = api.moe_route(ld_, cfg.k)
-    counts = torch.bincount(idx_d.reshape(-1).long(), minlength=cfg.E)
-    active = int((counts > 0).sum())
-    wbytes = active * 3 * cfg.H * cfg.I * 2
-    dec_ms = float(np.median(dec))
-
+    a4 = cfg.act_fmt == "nvfp4"
+    launches = 8 + (2 if a4 else 0)  # route, 4 permute, 2 GEMM, combine (+ amax, quantise)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{cfg.name} moe layer bf16, T={T}", "H": cfg.H, "E": cfg.E, "k": cfg.k,
-                   "I": cfg.I, "T": T, "zipf": cfg.zipf, "seed": 0,
+        "metric": metric_name(cfg, T), "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4" if a4 else "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} moe layer, {cfg.w_fmt} weights, {cfg.act_fmt} activations, T={T}",
+                   "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "I_s": cfg.I_s, "T": T, "zipf": cfg.zipf,
+                   "seed": 0, "active_experts": active,
                    "l2": "flushed before every step (256 MB write, outside the events)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roofline,
+        "roofline": roof,
         "stage_ms": {n: round(float(np.mean(stage_ms[:, i])), 4) for i, n in
                      enumerate(["route", "quant", "permute", "gemm_gate_up", "gemm_down", "combine"])},
-        "e2e": {"value": round(world * T / e2e_s, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": 8 * args.steps,
+        "e2e": {"value": round(world * T / e2e_s, 1), "unit": UNIT,
+                "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 2},
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
-        "decode_T256": {"ms": round(dec_ms, 4), "tokens_per_s": round(Td / (dec_ms / 1e3), 1),
-                        "active_experts": active,
-                        "weight_gbs": round(wbytes / (dec_ms / 1e3) / 1e9, 1),
-                        "hbm_frac": round(wbytes / (dec_ms / 1e3) / 1e9 / p["hbm_gbs"], 4)},
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        w_host = (w.w13.cpu(), w.w2.cpu())
+
+    if is_main:
+        # decode-size point on the same weights (weight-streaming bound)
+        Td = T_DECODE
+        xd_, ld_, od_ = x[:Td].contiguous(), logits[:Td].contiguous(), out[:Td]
+        evd = new_events()
+        dec = []
+        for i in range(args.warmup + 10):
+            flush.zero_()
+            api.moe_forward_profiled(layer.c, xd_, ld_, od_, ws, evd)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                dec.append((evd[0].elapsed_time(evd[6]), evd[3].elapsed_time(evd[5])))
+        idx_d, _ = api.moe_route(ld_, cfg.k)
+        act_d = int((torch.bincount(idx_d.reshape(-1).long(), minlength=cfg.E) > 0).sum())
+        dec_ms = float(np.median([d[0] for d in dec]))
+        dec_gemm = float(np.median([d[1] for d in dec]))
+        line["decode_T256"] = {"ms": round(dec_ms, 4), "tokens_per_s": round(Td / (dec_ms / 1e3), 1),
+                               "roofline": roofline(cfg, Td, dec_gemm, act_d, None, src)}
+    if keep_master:
+        if w_host is None:
+            w_host = (w.w13.cpu(), w.w2.cpu())
         toks = synth.sample_tokens(T, args.cpu_tokens, seed=1)
         r, dt = oracle_tokens_per_s(cfg, acts, w_host, toks)
         line["cpu_baseline"] = {"value": round(r, 3), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
@@ -378,10 +445,17 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=4096)
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="main", choices=["main", "small"],
                     help="main: the benchmark workload; small: the ncu profiling case")
+    ap.add_argument("--config", default=None, choices=list(synth.CONFIGS) + ["deepseek-v3-sweep"],
+                    help="measure another workload of synth/ instead of the benchmark one")
+    ap.add_argument("--T", type=int, default=None, help="tokens (default: the workload's largest)")
+    ap.add_argument("--zipf", type=float, default=None, help="router-bias Zipf exponent override")
+    ap.add_argument("--w-fmt", default=None, choices=["bf16", "nvfp4"], help="sweep weight format")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="profiling variant: this many experts, tokens scaled to keep tokens per expert")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -20,6 +20,10 @@ int check_launch();                 // MOE_OK or MOE_ERR_CUDA after a launch
 int num_sms();                      // SMs of the current device
 unsigned long long wait_timeout_ns();
 unsigned int* device_error_word();  // device address of the error word (current device)
+// 2-D TMA descriptor over a row-major [rows, inner] matrix of 2-byte (bf16)
+// or 1-byte elements; zero fill out of bounds; optional 128-byte swizzle.
+int encode_tmap_2d(CUtensorMap* m, const void* ptr, int elem_bytes, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                   uint32_t box_rows, bool swizzle128);
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -84,6 +88,21 @@ DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or about `hint_ns` nanoseconds pass (the thread stops issuing
+// while it waits).
+DEVINL bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Error word values (device side); the host maps them to MOE_ERR_TIMEOUT.
 constexpr unsigned int kErrTimeout = 1u;
 
@@ -93,9 +112,9 @@ constexpr unsigned int kErrTimeout = 1u;
 DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns,
                               unsigned int* err, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
     if (abort != nullptr && *abort) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       atomicOr(err, kErrTimeout);
@@ -103,6 +122,18 @@ DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long
       return false;
     }
   }
+}
+
+// The same wait for a whole warp: lane 0 waits (so one thread, not 32, polls
+// the barrier), then every lane observes the completed phase once, which
+// gives each lane the acquire ordering of the barrier.  Warp-uniform result.
+DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns, unsigned int* err,
+                           volatile int* abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, timeout_ns, err, abort) ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (ok) mbar_try_wait(bar, parity);
+  return ok != 0;
 }
 
 // ---- TMA
@@ -117,6 +148,24 @@ DEVINL void tma_load_2d(const void* tmap, uint64_t* bar, void* smem_dst, int x, 
       : "memory");
 }
 DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---- cp.async (4-byte asynchronous copies global -> shared)
+// Copies 4 bytes, or writes 4 zero bytes when `valid` is false (nothing is
+// read then; `src` must still be a valid global address).
+DEVINL void cp_async_4(uint32_t dst_smem, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst_smem), "l"(src), "r"(valid ? 4 : 0)
+               : "memory");
+}
+DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+DEVINL void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Arrive on `bar` once all cp.async of this thread issued so far complete
+// (the barrier's expected count includes this arrival).
+DEVINL void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // ---- tcgen05 (5th-generation tensor cores, tensor memory)
 DEVINL void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -139,6 +188,24 @@ DEVINL void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t i
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// D[tmem] (+)= (A * sfA) * (B * sfB)^T with packed E2M1 operands in shared
+// memory and one E4M3 scale per 16 elements along K, read from tensor memory
+// (kind::mxf4nvf4, block_scale, scale_vec::4X: K = 64 per instruction).
+DEVINL void umma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                      uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Copy 32 rows x 128 bits from shared memory into tensor memory, replicated
+// into the four 32-lane quadrants (row i -> lanes i, 32+i, 64+i, 96+i).
+DEVINL void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // Arrive on `bar` once every tcgen05 op issued so far by this thread completes.
 DEVINL void umma_commit(uint64_t* bar) {
@@ -173,6 +240,28 @@ DEVINL uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;                  // descriptor version for tcgen05
   d |= static_cast<uint64_t>(2) << 61;                  // swizzle mode: 128B
   return d;
+}
+
+// Shared-memory descriptor of a K-major operand without swizzle whose rows
+// are 16 bytes, stored contiguously (8-row core matrices 128 bytes apart):
+// the layout of a 32 x 128-bit block of scale factors for tcgen05.cp.
+DEVINL uint64_t smem_desc_kmajor_noswizzle_16B_rows(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (one core matrix along K)
+  d |= static_cast<uint64_t>(128 >> 4) << 32;           // stride byte offset: 8 rows * 16 B
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version for tcgen05
+  return d;                                              // swizzle mode 0: none
+}
+
+// Instruction descriptor, kind::mxf4nvf4 with block scaling: E2M1 x E2M1 ->
+// fp32, E4M3 scale factors (scale format bit 0), both operands K-major,
+// scale-factor ids 0, K = 64 per instruction.
+__host__ __device__ constexpr uint32_t idesc_nvf4_f32(int M, int N) {
+  return (1u << 7)                                  // A format E2M1
+         | (1u << 10)                               // B format E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
 // Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.

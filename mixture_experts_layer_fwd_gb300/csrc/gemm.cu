@@ -27,17 +27,14 @@
 // The SwiGLU epilogue needs gate and up of the same feature in one thread:
 // the B tile holds 128 gate rows followed by the matching 128 up rows, so
 // accumulator columns [0,128) are gate and [128,256) are up.
-#include <cudaTypedefs.h>
-
 #include <cstring>
 
+#include "gemm_common.cuh"
 #include "internal.h"
-#include "nvfp4.cuh"
 
 namespace moe {
 namespace gg {
 
-constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
@@ -46,79 +43,21 @@ constexpr int A_TILE = BM * BK * 2;   // 16 KB bf16
 constexpr int B_TILE = BN * BK * 2;   // 32 KB bf16
 constexpr int A_CODES = BM * BK / 2;  // 4 KB packed E2M1
 constexpr int B_CODES = BN * BK / 2;  // 8 KB packed E2M1
-constexpr int MAX_G = 1025;  // routed groups + the shared expert
-
-struct Prob {
-  int n_out;         // output columns N
-  int K;             // reduction length
-  int w_rows;        // weight rows per group (N, or 2N for SwiGLU)
-  int n_tiles;       // column blocks per group
-  int a_rows;        // rows of A (bounds of the scale loads)
-  int w_rows_total;  // rows of W over all groups
-  void* c;
-  uint8_t* c_sf;
-  const float* a_g;
-  const float* w_g;
-  const float* c_g;
-  const uint8_t* a_sf;
-  const uint8_t* w_sf;
-};
-
-struct Params {
-  CUtensorMap tma_a[2];  // [0] routed problem, [1] shared-expert problem
-  CUtensorMap tma_w[2];
-  Prob prob[2];
-  const int32_t* offsets;  // [G+1] rows of each routed group in A
-  int G;
-  int shared_rows;  // rows of the shared problem; < 0: none
-  unsigned int* err;
-  unsigned long long timeout_ns;
-};
-
 template <int EPI, bool A4, bool W4>
 struct Cfg {
   static constexpr bool CONV = A4 || W4;
   static constexpr int STAGES = CONV ? 3 : 4;
   static constexpr int STAGE_BYTES = A_TILE + B_TILE + (A4 ? A_CODES : 0) + (W4 ? B_CODES : 0);
-  static constexpr int NUM_WARPS = CONV ? 10 : 6;
+  static constexpr int NUM_WARPS = CONV ? 11 : 6;  // converters: warps 6..9, scale loader: warp 10
   static constexpr int THREADS = NUM_WARPS * 32;
   static constexpr int TILE_N = (EPI == MOE_EPI_STORE_BF16) ? 256 : 128;  // output columns per tile
   static constexpr uint32_t TX_BYTES = (A4 ? A_CODES : A_TILE) + (W4 ? B_CODES : B_TILE);
-  static constexpr int EXTRA = 2048 + 4 * (2 * MAX_G + 8) + 1024;
+  static constexpr int SF_RING_WORDS = 384;  // per stage: 128 A rows + 256 B rows, one 32-bit word each
+  static constexpr int EXTRA = 2048 + 4 * (2 * MAX_G + 8) + 1024 + (CONV ? STAGES * SF_RING_WORDS * 4 : 0);
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA;
   static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
-
-struct TileInfo {
-  int pb;     // problem: 0 routed, 1 shared
-  int g;      // group inside the problem
-  int row0;   // first row of the group in A / C
-  int rows;   // rows of the group
-  int m_blk;  // row block inside the group
-  int n_blk;  // column block
-};
-
-DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
-  int lo = 0, hi = GT;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s_prefix[mid] <= t) lo = mid; else hi = mid;
-  }
-  TileInfo ti;
-  const bool routed = lo < G;
-  ti.pb = routed ? 0 : 1;
-  ti.g = routed ? lo : 0;
-  ti.row0 = routed ? s_off[lo] : 0;
-  ti.rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
-  const int mt = (ti.rows + BM - 1) / BM;
-  const int local = t - s_prefix[lo];
-  ti.n_blk = local / mt;
-  ti.m_blk = local - ti.n_blk * mt;
-  return ti;
-}
-
-DEVINL float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // Converts one 64-element row of packed E2M1 codes (32 bytes in smem) with
 // its four E4M3 block scales into bf16, written into a 128-byte swizzled row.
@@ -152,7 +91,8 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
   uint64_t* full = reinterpret_cast<uint64_t*>(base + S * C::STAGE_BYTES);
   uint64_t* empty = full + S;
   uint64_t* conv = empty + S;
-  uint64_t* tfull = conv + S;
+  uint64_t* sf_full = conv + S;
+  uint64_t* tfull = sf_full + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -160,6 +100,7 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
   int* s_prefix = reinterpret_cast<int*>(base + S * C::STAGE_BYTES + 256);
   int* s_off = s_prefix + MAX_G + 4;
   uint32_t* lut = reinterpret_cast<uint32_t*>(s_off + MAX_G + 4);
+  uint32_t* sf_ring = lut + 256;  // [S][SF_RING_WORDS] E4M3 scale words of each stage
   __shared__ int warp_sums[32];
 
   const int warp = threadIdx.x >> 5;
@@ -172,6 +113,7 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&conv[s], 128);
+      mbar_init(&sf_full[s], 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -185,47 +127,12 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
-  // ---- tile schedule: prefix over per-group tile counts
-  for (int i = threadIdx.x; i <= G; i += C::THREADS) s_off[i] = p.offsets[i];
   if (C::CONV) {
     for (int b = threadIdx.x; b < 256; b += C::THREADS)
       lut[b] = e2m1_to_bf16_bits(b & 15u) | (e2m1_to_bf16_bits(b >> 4) << 16);
   }
-  __syncthreads();
-  {
-    const int per = (GT + C::THREADS - 1) / C::THREADS;
-    const int g0 = threadIdx.x * per;
-    int local = 0;
-    for (int g = g0; g < min(GT, g0 + per); ++g) {
-      const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
-      local += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
-    }
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int v = (lane < C::NUM_WARPS) ? warp_sums[lane] : 0;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xFFFFFFFFu, v, off);
-        if (lane >= off) v += o;
-      }
-      warp_sums[lane] = v;
-    }
-    __syncthreads();
-    int run = incl - local + (warp ? warp_sums[warp - 1] : 0);
-    for (int g = g0; g < min(GT, g0 + per); ++g) {
-      s_prefix[g] = run;
-      const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
-      run += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
-    }
-    if (threadIdx.x == 0) s_prefix[GT] = warp_sums[C::NUM_WARPS - 1];
-  }
+  // ---- tile schedule: prefix over per-group tile counts
+  build_schedule<C::THREADS, C::NUM_WARPS>(p, s_off, s_prefix, warp_sums);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -344,77 +251,17 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
       const Prob& P = p.prob[ti.pb];
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
-      if (!mbar_wait_bounded(&tfull[buf], use & 1u, tmo, p.err, abort_flag)) break;
+      if (!mbar_wait_warp(&tfull[buf], use & 1u, tmo, p.err, abort_flag)) break;
       tc_fence_after();
-      const int m_local = ti.m_blk * BM + r_in_tile;
-      const bool valid = m_local < ti.rows;
-      const size_t row = static_cast<size_t>(ti.row0) + m_local;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
       float scale = 1.0f;
       if (A4) scale *= __ldg(P.a_g);
       if (W4) scale *= __ldg(P.w_g + ti.g);
-      if (EPI == MOE_EPI_STORE_BF16) {
-#pragma unroll 1
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + cc * 32, r);
-          tmem_ld_wait();
-          const int col = ti.n_blk * BN + cc * 32;
-          if (valid && col < P.n_out) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.c) + row * P.n_out + col);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * scale, __uint_as_float(r[8 * v + 1]) * scale);
-              o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * scale, __uint_as_float(r[8 * v + 3]) * scale);
-              o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * scale, __uint_as_float(r[8 * v + 5]) * scale);
-              o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * scale, __uint_as_float(r[8 * v + 7]) * scale);
-              dst[v] = o;
-            }
-          }
-        }
-      } else {
-        const float cg = (EPI == MOE_EPI_SWIGLU_NVFP4) ? __ldg(P.c_g) : 1.0f;
-#pragma unroll 1
-        for (int cc = 0; cc < 128 / 32; ++cc) {
-          uint32_t rg[32], ru[32];
-          tmem_ld_32x32b_x32(taddr + cc * 32, rg);
-          tmem_ld_32x32b_x32(taddr + 128 + cc * 32, ru);
-          tmem_ld_wait();
-          const int col = ti.n_blk * 128 + cc * 32;
-          if (valid && col < P.n_out) {
-            float h[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              h[i] = silu_f(__uint_as_float(rg[i]) * scale) * (__uint_as_float(ru[i]) * scale);
-            if (EPI == MOE_EPI_SWIGLU_BF16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.c) + row * P.n_out + col);
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[v] = make_uint4(pack_bf16x2(h[8 * v], h[8 * v + 1]), pack_bf16x2(h[8 * v + 2], h[8 * v + 3]),
-                                    pack_bf16x2(h[8 * v + 4], h[8 * v + 5]), pack_bf16x2(h[8 * v + 6], h[8 * v + 7]));
-            } else {
-              float b0[16], b1[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                b0[i] = h[i];
-                b1[i] = h[16 + i];
-              }
-              uint32_t c0[2], c1[2];
-              const uint32_t s0 = nvfp4_quantize16(b0, cg, c0);
-              const uint32_t s1 = nvfp4_quantize16(b1, cg, c1);
-              uint8_t* cdst = static_cast<uint8_t*>(P.c) + row * (P.n_out / 2) + col / 2;
-              *reinterpret_cast<uint4*>(cdst) = make_uint4(c0[0], c0[1], c1[0], c1[1]);
-              *reinterpret_cast<uint16_t*>(P.c_sf + row * (P.n_out / 16) + col / 16) =
-                  static_cast<uint16_t>(s0 | (s1 << 8));
-            }
-          }
-        }
-      }
+      epilogue_tile<EPI, BN>(P, ti, taddr, r_in_tile, scale);
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }
-  } else if (C::CONV) {
+  } else if (C::CONV && warp < 10) {
     // ===================================================== NVFP4 -> bf16 converters
     const int ct = threadIdx.x - 6 * 32;  // 0..127
     int stage = 0;
@@ -422,37 +269,21 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const TileInfo ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
-      const Prob& P = p.prob[ti.pb];
-      const int a_y = ti.row0 + ti.m_blk * BM;
-      const int w_y0 = ti.g * P.w_rows + ti.n_blk * C::TILE_N;
-      const int w_y1 = (EPI == MOE_EPI_STORE_BF16) ? w_y0 + 128 : w_y0 + P.n_out;
-      const int nk = P.K / BK;
-      const int sf_ld = P.K / 16;
+      const int nk = p.prob[ti.pb].K / BK;
       for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait_bounded(&full[stage], phase, tmo, p.err, abort_flag)) {
+        if (!mbar_wait_warp(&full[stage], phase, tmo, p.err, abort_flag) ||
+            !mbar_wait_warp(&sf_full[stage], phase, tmo, p.err, abort_flag)) {
           ok = false;
           break;
         }
         uint8_t* sb = stages + stage * C::STAGE_BYTES;
-        if (A4) {
-          const int grow = a_y + ct;
-          const uint32_t sfw =
-              (grow < P.a_rows)
-                  ? __ldg(reinterpret_cast<const uint32_t*>(P.a_sf + static_cast<size_t>(grow) * sf_ld + kb * 4))
-                  : 0u;
-          convert_row(sb + A_TILE + B_TILE + ct * 32, sfw, sb, ct, lut);
-        }
+        const uint32_t* sfw = sf_ring + stage * C::SF_RING_WORDS;
+        if (A4) convert_row(sb + A_TILE + B_TILE + ct * 32, sfw[ct], sb, ct, lut);
         if (W4) {
           const uint8_t* wc = sb + A_TILE + B_TILE + (A4 ? A_CODES : 0);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int grow = (h ? w_y1 : w_y0) + ct;
-            const uint32_t sfw =
-                (grow < P.w_rows_total)
-                    ? __ldg(reinterpret_cast<const uint32_t*>(P.w_sf + static_cast<size_t>(grow) * sf_ld + kb * 4))
-                    : 0u;
-            convert_row(wc + (h * 128 + ct) * 32, sfw, sb + A_TILE, h * 128 + ct, lut);
-          }
+          for (int h = 0; h < 2; ++h)
+            convert_row(wc + (h * 128 + ct) * 32, sfw[128 + h * 128 + ct], sb + A_TILE, h * 128 + ct, lut);
         }
         fence_proxy_async_smem();
         mbar_arrive(&conv[stage]);
@@ -462,6 +293,56 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
         }
       }
     }
+  } else if (C::CONV) {
+    // ===================================================== scale loader (warp 10)
+    // Asynchronous 4-byte copies of each stage's E4M3 scale words (one word =
+    // the 4 block scales of a row over the stage's 64 elements) into the
+    // stage's ring slot; each lane's copies arrive on sf_full when they land,
+    // so several stages of scales are in flight while the converters work.
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileInfo ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const Prob& P = p.prob[ti.pb];
+      const int a_y = ti.row0 + ti.m_blk * BM;
+      const int w_y0 = ti.g * P.w_rows + ti.n_blk * C::TILE_N;
+      const int w_y1 = (EPI == MOE_EPI_STORE_BF16) ? w_y0 + 128 : w_y0 + P.n_out;
+      const int nk = P.K / BK;
+      const int sf_ld = P.K / 16;
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_warp(&empty[stage], phase ^ 1u, tmo, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t ring = smem_u32(sf_ring + stage * C::SF_RING_WORDS);
+        if (A4) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            const int grow = a_y + r;
+            const bool v = grow < P.a_rows;
+            cp_async_4(ring + 4 * r, v ? P.a_sf + static_cast<size_t>(grow) * sf_ld + kb * 4 : P.a_sf, v);
+          }
+        }
+        if (W4) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = lane + 32 * i;
+            const int grow = (r < 128) ? w_y0 + r : w_y1 + (r - 128);
+            const bool v = grow < P.w_rows_total;
+            cp_async_4(ring + 4 * (128 + r), v ? P.w_sf + static_cast<size_t>(grow) * sf_ld + kb * 4 : P.w_sf, v);
+          }
+        }
+        cp_async_mbar_arrive(&sf_full[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    cp_async_wait_group<0>();
   }
 
   tc_fence_before();
@@ -473,32 +354,11 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
 }
 
 // ------------------------------------------------------------------ host
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
-    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-// 2-D tensor map over a row-major [rows, inner] matrix.
+// 2-D tensor map over a row-major [rows, inner] matrix: bf16 with the
+// 128-byte swizzle, or packed E2M1 bytes without swizzle (converter path).
 static int make_map(CUtensorMap* m, const void* ptr, bool bf16, uint64_t inner, uint64_t rows, uint32_t box_inner,
                     uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return MOE_ERR_CUDA;
-  const uint64_t esize = bf16 ? 2 : 1;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * esize};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr),
-                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+  return encode_tmap_2d(m, ptr, bf16 ? 2 : 1, inner, rows, box_inner, box_rows, bf16);
 }
 
 }  // namespace gg
@@ -573,6 +433,7 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
   // routed rows are T*k >= T shared rows, so an empty routed problem means
   // there is nothing to do
   if (routed.a_rows == 0) return MOE_OK;
+  if (a4 && w4) return grouped_gemm_launch_nvf4(epi, routed, offsets, G, sh, shared_rows, s);
   const bool have_shared = sh != nullptr && shared_rows > 0;
   gg::Params prm;
   memset(&prm, 0, sizeof(prm));
@@ -593,10 +454,6 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
   } else if (!a4 && w4) {
     if (epi == MOE_EPI_STORE_BF16) return launch_impl<MOE_EPI_STORE_BF16, false, true>(prm, s);
     if (epi == MOE_EPI_SWIGLU_BF16) return launch_impl<MOE_EPI_SWIGLU_BF16, false, true>(prm, s);
-  } else {
-    if (epi == MOE_EPI_STORE_BF16) return launch_impl<MOE_EPI_STORE_BF16, true, true>(prm, s);
-    if (epi == MOE_EPI_SWIGLU_BF16) return launch_impl<MOE_EPI_SWIGLU_BF16, true, true>(prm, s);
-    if (epi == MOE_EPI_SWIGLU_NVFP4) return launch_impl<MOE_EPI_SWIGLU_NVFP4, true, true>(prm, s);
   }
   return MOE_ERR_UNSUPPORTED;
 }

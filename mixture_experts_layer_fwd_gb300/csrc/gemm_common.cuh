@@ -1,0 +1,193 @@
+// Pieces shared by the grouped-GEMM kernels: problem description, the
+// persistent tile schedule over ragged groups, and the epilogues that turn a
+// tensor-memory accumulator tile into the layer's outputs.
+#pragma once
+
+#include "nvfp4.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = 128;       // rows (tokens) per tile = MMA M
+constexpr int MAX_G = 1025;   // routed groups + the shared expert
+
+struct Prob {
+  int n_out;         // output columns N
+  int K;             // reduction length
+  int w_rows;        // weight rows per group (N, or 2N for SwiGLU)
+  int n_tiles;       // column blocks per group
+  int a_rows;        // rows of A (bounds of the scale loads)
+  int w_rows_total;  // rows of W over all groups
+  void* c;
+  uint8_t* c_sf;
+  const float* a_g;
+  const float* w_g;
+  const float* c_g;
+  const uint8_t* a_sf;
+  const uint8_t* w_sf;
+};
+
+struct Params {
+  CUtensorMap tma_a[2];  // [0] routed problem, [1] shared-expert problem
+  CUtensorMap tma_w[2];
+  CUtensorMap tma_asf[2];  // scale rows of A / W (block-scaled kernel, when sf_tma)
+  CUtensorMap tma_wsf[2];
+  Prob prob[2];
+  const int32_t* offsets;  // [G+1] rows of each routed group in A
+  int G;
+  int shared_rows;  // rows of the shared problem; < 0: none
+  int sf_tma;       // block-scaled kernel: scale rows arrive by TMA (K % 256 == 0 everywhere)
+  unsigned int* err;
+  unsigned long long timeout_ns;
+};
+
+struct TileInfo {
+  int pb;     // problem: 0 routed, 1 shared
+  int g;      // group inside the problem
+  int row0;   // first row of the group in A / C
+  int rows;   // rows of the group
+  int m_blk;  // row block inside the group
+  int n_blk;  // column block
+};
+
+// Tile t -> (group, column block, row block), row blocks fastest.  s_prefix
+// holds the exclusive prefix of tiles per group (GT+1 entries).
+DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
+  int lo = 0, hi = GT;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  const bool routed = lo < G;
+  ti.pb = routed ? 0 : 1;
+  ti.g = routed ? lo : 0;
+  ti.row0 = routed ? s_off[lo] : 0;
+  ti.rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
+  const int mt = (ti.rows + BM - 1) / BM;
+  const int local = t - s_prefix[lo];
+  ti.n_blk = local / mt;
+  ti.m_blk = local - ti.n_blk * mt;
+  return ti;
+}
+
+// Loads the group offsets and builds the per-group tile prefix in shared
+// memory.  Called by every thread of the block (contains barriers).
+template <int THREADS, int NUM_WARPS>
+DEVINL void build_schedule(const Params& p, int* s_off, int* s_prefix, int* warp_sums) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  const int GT = G + (p.shared_rows >= 0 ? 1 : 0);
+  for (int i = threadIdx.x; i <= G; i += THREADS) s_off[i] = p.offsets[i];
+  __syncthreads();
+  const int per = (GT + THREADS - 1) / THREADS;
+  const int g0 = threadIdx.x * per;
+  int local = 0;
+  for (int g = g0; g < min(GT, g0 + per); ++g) {
+    const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
+    local += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
+  }
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = (lane < NUM_WARPS) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+      if (lane >= off) v += o;
+    }
+    warp_sums[lane] = v;
+  }
+  __syncthreads();
+  int run = incl - local + (warp ? warp_sums[warp - 1] : 0);
+  for (int g = g0; g < min(GT, g0 + per); ++g) {
+    s_prefix[g] = run;
+    const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
+    run += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
+  }
+  if (threadIdx.x == 0) s_prefix[GT] = warp_sums[NUM_WARPS - 1];
+}
+
+DEVINL float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+// Epilogue of one tile held in tensor memory: ACC_N fp32 columns per row.
+// STORE: C[row, n_blk*ACC_N + c] = bf16(scale * acc[c]).
+// SWIGLU: columns [0, ACC_N/2) are gate, [ACC_N/2, ACC_N) up of the same
+// features; C[row, n_blk*ACC_N/2 + c] = silu(scale*g) * (scale*u), stored as
+// bf16 or quantised to NVFP4 with global scale *P.c_g.
+// Every lane of the warp must call it (tcgen05.ld is warp-collective); only
+// rows inside the tile's group are stored.
+template <int EPI, int ACC_N>
+DEVINL void epilogue_tile(const Prob& P, const TileInfo& ti, uint32_t taddr, int r_in_tile, float scale) {
+  const int m_local = ti.m_blk * BM + r_in_tile;
+  const bool valid = m_local < ti.rows;
+  const size_t row = static_cast<size_t>(ti.row0) + m_local;
+  if (EPI == MOE_EPI_STORE_BF16) {
+#pragma unroll 1
+    for (int cc = 0; cc < ACC_N / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + cc * 32, r);
+      tmem_ld_wait();
+      const int col = ti.n_blk * ACC_N + cc * 32;
+      if (valid && col < P.n_out) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.c) + row * P.n_out + col);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * scale, __uint_as_float(r[8 * v + 1]) * scale);
+          o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * scale, __uint_as_float(r[8 * v + 3]) * scale);
+          o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * scale, __uint_as_float(r[8 * v + 5]) * scale);
+          o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * scale, __uint_as_float(r[8 * v + 7]) * scale);
+          dst[v] = o;
+        }
+      }
+    }
+  } else {
+    constexpr int HALF = ACC_N / 2;
+    const float cg = (EPI == MOE_EPI_SWIGLU_NVFP4) ? __ldg(P.c_g) : 1.0f;
+#pragma unroll 1
+    for (int cc = 0; cc < HALF / 32; ++cc) {
+      uint32_t rg[32], ru[32];
+      tmem_ld_32x32b_x32(taddr + cc * 32, rg);
+      tmem_ld_32x32b_x32(taddr + HALF + cc * 32, ru);
+      tmem_ld_wait();
+      const int col = ti.n_blk * HALF + cc * 32;
+      if (valid && col < P.n_out) {
+        float h[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          h[i] = silu_f(__uint_as_float(rg[i]) * scale) * (__uint_as_float(ru[i]) * scale);
+        if (EPI == MOE_EPI_SWIGLU_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.c) + row * P.n_out + col);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pack_bf16x2(h[8 * v], h[8 * v + 1]), pack_bf16x2(h[8 * v + 2], h[8 * v + 3]),
+                                pack_bf16x2(h[8 * v + 4], h[8 * v + 5]), pack_bf16x2(h[8 * v + 6], h[8 * v + 7]));
+        } else {
+          float b0[16], b1[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            b0[i] = h[i];
+            b1[i] = h[16 + i];
+          }
+          uint32_t c0[2], c1[2];
+          const uint32_t s0 = nvfp4_quantize16(b0, cg, c0);
+          const uint32_t s1 = nvfp4_quantize16(b1, cg, c1);
+          uint8_t* cdst = static_cast<uint8_t*>(P.c) + row * (P.n_out / 2) + col / 2;
+          *reinterpret_cast<uint4*>(cdst) = make_uint4(c0[0], c0[1], c1[0], c1[1]);
+          *reinterpret_cast<uint16_t*>(P.c_sf + row * (P.n_out / 16) + col / 16) =
+              static_cast<uint16_t>(s0 | (s1 << 8));
+        }
+      }
+    }
+  }
+}
+
+}  // namespace gg
+}  // namespace moe

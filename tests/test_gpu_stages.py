@@ -270,6 +270,30 @@ def test_grouped_gemm_nvfp4_weights():
     assert err < 5e-3, err
 
 
+@pytest.mark.parametrize("epi,N,K", [(0, 384, 320), (1, 192, 576), (0, 256, 1024), (1, 128, 256)])
+def test_grouped_gemm_nvfp4_both_block_scaled(epi, N, K):
+    """NVFP4 A x NVFP4 W on the block-scaled FP4 MMA, bf16 outputs; K tails
+    that are not multiples of the 256-element stage; ragged and empty groups."""
+    m = api()
+    counts = [0, 1, 127, 129, 300, 0, 40]
+    offs = _ragged_offsets(counts)
+    M, G = int(offs[-1]), len(counts)
+    Wn = N if epi == 0 else 2 * N
+    g = torch.Generator().manual_seed(N + K + epi)
+    Aq, As, Ag = nvfp4.quantize(torch.randn(M, K, generator=g).numpy())
+    Wq = [nvfp4.quantize((torch.randn(Wn, K, generator=g) * 0.02).numpy()) for _ in range(G)]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    C = m.moe_grouped_gemm(1, 1, epi, offs.to(DEV), N, K, t(Aq), t(np.stack([q for q, _, _ in Wq])), A_sf=t(As),
+                           A_g=torch.tensor([Ag], device=DEV), W_sf=t(np.stack([s for _, s, _ in Wq])),
+                           W_g=torch.tensor([gg for _, _, gg in Wq], dtype=torch.float32, device=DEV))
+    _sync()
+    Ad = nvfp4.dequantize(Aq, As, Ag)
+    Wd = np.stack([nvfp4.dequantize(q, s, gg) for q, s, gg in Wq])
+    ref = _gemm_ref(Ad, Wd, offs.numpy(), epi == 1, N)
+    err = oracle.rel_frobenius(C.float().cpu().numpy(), ref)
+    assert err < 5e-3, err
+
+
 def test_grouped_gemm_nvfp4_both_with_nvfp4_output():
     """NVFP4 A x NVFP4 W, SwiGLU output quantised to NVFP4 with a given scale."""
     m = api()
