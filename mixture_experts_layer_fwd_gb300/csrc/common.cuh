@@ -109,12 +109,15 @@ constexpr unsigned int kErrTimeout = 1u;
 // Bounded wait on an mbarrier phase.  Gives up after `timeout_ns` of wall
 // time (or as soon as *abort is set by another role of the block), records
 // kErrTimeout in *err and returns false.
+// `suspend`: let the hardware park the thread while it waits (for warps that
+// are idle anyway); otherwise poll, for the latency-critical single-thread
+// roles (TMA producer, MMA issuer).
 DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns,
-                              unsigned int* err, volatile int* abort) {
+                              unsigned int* err, volatile int* abort, bool suspend = false) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
+    if (suspend ? mbar_try_wait_suspend(bar, parity, 100000u) : mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       atomicOr(err, kErrTimeout);
@@ -130,7 +133,7 @@ DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned long long
 DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns, unsigned int* err,
                            volatile int* abort) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, timeout_ns, err, abort) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, timeout_ns, err, abort, true) ? 1 : 0;
   ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
   if (ok) mbar_try_wait(bar, parity);
   return ok != 0;

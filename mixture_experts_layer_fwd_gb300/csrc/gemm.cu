@@ -18,10 +18,14 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulators, SwiGLU / scaling /
 //               bf16 or NVFP4 rounding, stores of the rows of the tile that
 //               belong to the tile's group
-//   warps 6..9  (NVFP4 operands only) converters: packed E2M1 codes x E4M3
-//               scale -> bf16 into the swizzled operand tile.  e2m1 * e4m3 is
-//               exact in bf16, so the bf16 MMA computes exactly the NVFP4
-//               products; the fp32 global scales are applied in the epilogue.
+//   warps 6..13 (NVFP4 operands only) converters, one operand row per thread:
+//               packed E2M1 codes x E4M3 scale -> bf16 into the swizzled
+//               operand tile, through a byte -> bf16x2 table replicated per
+//               lane (conflict-free lookups).  e2m1 * e4m3 is exact in bf16,
+//               so the bf16 MMA computes exactly the NVFP4 products; the fp32
+//               global scales are applied in the epilogue
+//   warp 14     (NVFP4 operands only) scale loader: cp.async of each stage's
+//               E4M3 scale words into a small ring, tracked by an mbarrier
 // Tiles are (group, n-block, m-block) with m fastest; group sizes are read
 // on the device (offsets), so nothing is synchronised with the host.
 // The SwiGLU epilogue needs gate and up of the same feature in one thread:
@@ -48,12 +52,18 @@ struct Cfg {
   static constexpr bool CONV = A4 || W4;
   static constexpr int STAGES = CONV ? 3 : 4;
   static constexpr int STAGE_BYTES = A_TILE + B_TILE + (A4 ? A_CODES : 0) + (W4 ? B_CODES : 0);
-  static constexpr int NUM_WARPS = CONV ? 11 : 6;  // converters: warps 6..9, scale loader: warp 10
+  static constexpr int CONV_WARPS = 8;  // converters: warps 6..13, one operand row per thread
+  static constexpr int SF_WARP = 6 + CONV_WARPS;
+  static constexpr int NUM_WARPS = CONV ? SF_WARP + 1 : 6;  // + scale loader
   static constexpr int THREADS = NUM_WARPS * 32;
   static constexpr int TILE_N = (EPI == MOE_EPI_STORE_BF16) ? 256 : 128;  // output columns per tile
   static constexpr uint32_t TX_BYTES = (A4 ? A_CODES : A_TILE) + (W4 ? B_CODES : B_TILE);
   static constexpr int SF_RING_WORDS = 384;  // per stage: 128 A rows + 256 B rows, one 32-bit word each
-  static constexpr int EXTRA = 2048 + 4 * (2 * MAX_G + 8) + 1024 + (CONV ? STAGES * SF_RING_WORDS * 4 : 0);
+  // byte -> two bf16 table, one copy per lane (lut[byte][lane]): lookups with
+  // random bytes never collide on a bank
+  static constexpr int LUT_WORDS = CONV ? 256 * 32 : 0;
+  static constexpr int EXTRA =
+      2048 + 4 * (2 * MAX_G + 8) + 4 * LUT_WORDS + (CONV ? STAGES * SF_RING_WORDS * 4 : 0);
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA;
   static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -61,7 +71,7 @@ struct Cfg {
 
 // Converts one 64-element row of packed E2M1 codes (32 bytes in smem) with
 // its four E4M3 block scales into bf16, written into a 128-byte swizzled row.
-DEVINL void convert_row(const uint8_t* codes, uint32_t sfw, uint8_t* tile, int row, const uint32_t* lut) {
+DEVINL void convert_row(const uint8_t* codes, uint32_t sfw, uint8_t* tile, int row, const uint32_t* lut_lane) {
   const uint4 c0 = *reinterpret_cast<const uint4*>(codes);
   const uint4 c1 = *reinterpret_cast<const uint4*>(codes + 16);
   const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -72,7 +82,7 @@ DEVINL void convert_row(const uint8_t* codes, uint32_t sfw, uint8_t* tile, int r
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint32_t lv = lut[(cw[ch] >> (8 * q)) & 0xFFu];
+      uint32_t lv = lut_lane[((cw[ch] >> (8 * q)) & 0xFFu) * 32];
       __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&lv);
       v = __hmul2(v, s2);
       o[q] = *reinterpret_cast<uint32_t*>(&v);
@@ -100,7 +110,7 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
   int* s_prefix = reinterpret_cast<int*>(base + S * C::STAGE_BYTES + 256);
   int* s_off = s_prefix + MAX_G + 4;
   uint32_t* lut = reinterpret_cast<uint32_t*>(s_off + MAX_G + 4);
-  uint32_t* sf_ring = lut + 256;  // [S][SF_RING_WORDS] E4M3 scale words of each stage
+  uint32_t* sf_ring = lut + C::LUT_WORDS;  // [S][SF_RING_WORDS] E4M3 scale words of each stage
   __shared__ int warp_sums[32];
 
   const int warp = threadIdx.x >> 5;
@@ -112,7 +122,7 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&conv[s], 128);
+      mbar_init(&conv[s], C::CONV_WARPS * 32);
       mbar_init(&sf_full[s], 32);
     }
     for (int b = 0; b < 2; ++b) {
@@ -128,8 +138,10 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
     tmem_relinquish();
   }
   if (C::CONV) {
-    for (int b = threadIdx.x; b < 256; b += C::THREADS)
-      lut[b] = e2m1_to_bf16_bits(b & 15u) | (e2m1_to_bf16_bits(b >> 4) << 16);
+    for (int i = threadIdx.x; i < C::LUT_WORDS; i += C::THREADS) {
+      const uint32_t b = static_cast<uint32_t>(i) >> 5;
+      lut[i] = e2m1_to_bf16_bits(b & 15u) | (e2m1_to_bf16_bits(b >> 4) << 16);
+    }
   }
   // ---- tile schedule: prefix over per-group tile counts
   build_schedule<C::THREADS, C::NUM_WARPS>(p, s_off, s_prefix, warp_sums);
@@ -261,9 +273,10 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }
-  } else if (C::CONV && warp < 10) {
+  } else if (C::CONV && warp < C::SF_WARP) {
     // ===================================================== NVFP4 -> bf16 converters
-    const int ct = threadIdx.x - 6 * 32;  // 0..127
+    const int ct = threadIdx.x - 6 * 32;  // 0..255: one B row (and, below 128, one A row)
+    const uint32_t* lut_lane = lut + lane;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -278,12 +291,10 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
         }
         uint8_t* sb = stages + stage * C::STAGE_BYTES;
         const uint32_t* sfw = sf_ring + stage * C::SF_RING_WORDS;
-        if (A4) convert_row(sb + A_TILE + B_TILE + ct * 32, sfw[ct], sb, ct, lut);
+        if (A4 && ct < BM) convert_row(sb + A_TILE + B_TILE + ct * 32, sfw[ct], sb, ct, lut_lane);
         if (W4) {
           const uint8_t* wc = sb + A_TILE + B_TILE + (A4 ? A_CODES : 0);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            convert_row(wc + (h * 128 + ct) * 32, sfw[128 + h * 128 + ct], sb + A_TILE, h * 128 + ct, lut);
+          convert_row(wc + ct * 32, sfw[128 + ct], sb + A_TILE, ct, lut_lane);
         }
         fence_proxy_async_smem();
         mbar_arrive(&conv[stage]);
@@ -294,7 +305,7 @@ __global__ void __launch_bounds__(Cfg<EPI, A4, W4>::THREADS, 1) grouped_gemm_ker
       }
     }
   } else if (C::CONV) {
-    // ===================================================== scale loader (warp 10)
+    // ===================================================== scale loader (warp SF_WARP)
     // Asynchronous 4-byte copies of each stage's E4M3 scale words (one word =
     // the 4 block scales of a row over the stage's 64 elements) into the
     // stage's ring slot; each lane's copies arrive on sf_full when they land,
