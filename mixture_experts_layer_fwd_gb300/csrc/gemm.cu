@@ -445,6 +445,7 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
   // there is nothing to do
   if (routed.a_rows == 0) return MOE_OK;
   if (a4 && w4) return grouped_gemm_launch_nvf4(epi, routed, offsets, G, sh, shared_rows, s);
+  if (!a4 && !w4) return grouped_gemm_launch_pair(epi, routed, offsets, G, sh, shared_rows, s);
   const bool have_shared = sh != nullptr && shared_rows > 0;
   gg::Params prm;
   memset(&prm, 0, sizeof(prm));
@@ -459,10 +460,10 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
   prm.err = device_error_word();
   if (!prm.err) return MOE_ERR_CUDA;
   prm.timeout_ns = wait_timeout_ns();
-  if (!a4 && !w4) {
-    if (epi == MOE_EPI_STORE_BF16) return launch_impl<MOE_EPI_STORE_BF16, false, false>(prm, s);
-    if (epi == MOE_EPI_SWIGLU_BF16) return launch_impl<MOE_EPI_SWIGLU_BF16, false, false>(prm, s);
-  } else if (!a4 && w4) {
+  // bf16 x bf16 went to the CTA-pair kernel and NVFP4 x NVFP4 to the
+  // block-scaled kernel above; this kernel serves NVFP4 weights with bf16
+  // activations (converted to bf16 in shared memory)
+  if (!a4 && w4) {
     if (epi == MOE_EPI_STORE_BF16) return launch_impl<MOE_EPI_STORE_BF16, false, true>(prm, s);
     if (epi == MOE_EPI_SWIGLU_BF16) return launch_impl<MOE_EPI_SWIGLU_BF16, false, true>(prm, s);
   }

@@ -51,7 +51,9 @@ struct TileInfo {
 };
 
 // Tile t -> (group, column block, row block), row blocks fastest.  s_prefix
-// holds the exclusive prefix of tiles per group (GT+1 entries).
+// holds the exclusive prefix of tiles per group (GT+1 entries); TM is the
+// number of rows per tile (128, or 256 for the 2-SM kernel's pair tiles).
+template <int TM = BM>
 DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
   int lo = 0, hi = GT;
   while (hi - lo > 1) {
@@ -64,7 +66,7 @@ DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT
   ti.g = routed ? lo : 0;
   ti.row0 = routed ? s_off[lo] : 0;
   ti.rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
-  const int mt = (ti.rows + BM - 1) / BM;
+  const int mt = (ti.rows + TM - 1) / TM;
   const int local = t - s_prefix[lo];
   ti.n_blk = local / mt;
   ti.m_blk = local - ti.n_blk * mt;
@@ -73,7 +75,7 @@ DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT
 
 // Loads the group offsets and builds the per-group tile prefix in shared
 // memory.  Called by every thread of the block (contains barriers).
-template <int THREADS, int NUM_WARPS>
+template <int THREADS, int NUM_WARPS, int TM = BM>
 DEVINL void build_schedule(const Params& p, int* s_off, int* s_prefix, int* warp_sums) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
@@ -85,7 +87,7 @@ DEVINL void build_schedule(const Params& p, int* s_off, int* s_prefix, int* warp
   int local = 0;
   for (int g = g0; g < min(GT, g0 + per); ++g) {
     const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
-    local += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
+    local += ((rows + TM - 1) / TM) * p.prob[g < G ? 0 : 1].n_tiles;
   }
   int incl = local;
 #pragma unroll
@@ -109,7 +111,7 @@ DEVINL void build_schedule(const Params& p, int* s_off, int* s_prefix, int* warp
   for (int g = g0; g < min(GT, g0 + per); ++g) {
     s_prefix[g] = run;
     const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
-    run += ((rows + BM - 1) / BM) * p.prob[g < G ? 0 : 1].n_tiles;
+    run += ((rows + TM - 1) / TM) * p.prob[g < G ? 0 : 1].n_tiles;
   }
   if (threadIdx.x == 0) s_prefix[GT] = warp_sums[NUM_WARPS - 1];
 }

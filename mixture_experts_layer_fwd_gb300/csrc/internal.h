@@ -37,6 +37,10 @@ struct GemmProblem {
 int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed, const int32_t* offsets, int G,
                         const GemmProblem* sh, int shared_rows, cudaStream_t s);
 
+// Both operands bf16: MMA over CTA pairs (gemm_pair.cu).
+int grouped_gemm_launch_pair(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
+                             const GemmProblem* sh, int shared_rows, cudaStream_t s);
+
 // Both operands NVFP4: block-scaled FP4 tensor-core kernel (gemm_fp4.cu).
 int grouped_gemm_launch_nvf4(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                              const GemmProblem* sh, int shared_rows, cudaStream_t s);
