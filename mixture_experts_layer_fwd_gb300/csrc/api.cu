@@ -84,6 +84,41 @@ int encode_tmap_2d(CUtensorMap* m, const void* ptr, int elem_bytes, uint64_t inn
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
+// bf16 [rows, K] viewed as [K/64 k-blocks][rows][64]: a box {64, box_rows,
+// kblocks} at (0, r, kb) stages k-blocks kb.. of rows r.. as consecutive
+// 128-byte-row tiles (one per k-block), 128-byte swizzle.
+int encode_tmap_kblocks(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint32_t box_rows,
+                        uint32_t kblocks) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  cuuint64_t dims[3] = {64, rows, K / 64};
+  cuuint64_t strides[2] = {K * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, kblocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+// bf16 SwiGLU weights [groups][gate N rows | up N rows][K] viewed as
+// [K/64 k-blocks][2*groups][N][64]: a box {64, box_rows, 2, kblocks} at
+// (0, f, 2g, kb) stages, per k-block, rows f.. of group g's gate half
+// followed by the same rows of its up half.
+int encode_tmap_gateup(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t N, uint64_t groups,
+                       uint32_t box_rows, uint32_t kblocks) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  cuuint64_t dims[4] = {64, N, 2 * groups, K / 64};
+  cuuint64_t strides[3] = {K * 2, N * K * 2, 128};
+  cuuint32_t box[4] = {64, box_rows, 2, kblocks};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 __global__ void selftest_wait_kernel(unsigned int* err, unsigned long long timeout_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {

@@ -24,6 +24,16 @@ unsigned int* device_error_word();  // device address of the error word (current
 // or 1-byte elements; zero fill out of bounds; optional 128-byte swizzle.
 int encode_tmap_2d(CUtensorMap* m, const void* ptr, int elem_bytes, uint64_t inner, uint64_t rows, uint32_t box_inner,
                    uint32_t box_rows, bool swizzle128);
+// bf16 [rows, K] (K % 64 == 0) as k-blocks of 64: a box at (0, r, kb)
+// stages `kblocks` consecutive 64-wide k-blocks of box_rows rows, each as its
+// own 128-byte-swizzled tile (zero fill past the end of K or the rows).
+int encode_tmap_kblocks(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint32_t box_rows,
+                        uint32_t kblocks);
+// bf16 SwiGLU weights [groups][gate N | up N][K] as k-blocks: a box at
+// (0, f, 2g, kb) stages, per k-block, box_rows gate rows f.. of group g
+// followed by the same up rows.
+int encode_tmap_gateup(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t N, uint64_t groups,
+                       uint32_t box_rows, uint32_t kblocks);
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -182,6 +192,10 @@ DEVINL void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Named barrier `id` (1..15) over `threads` threads (a multiple of 32).
+DEVINL void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
 DEVINL void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
@@ -252,6 +266,21 @@ DEVINL void tma_load_2d_pair(const void* tmap, uint32_t bar_cluster_addr, void* 
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
       "%4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster_addr), "r"(x), "r"(y)
+      : "memory");
+}
+DEVINL void tma_load_3d_pair(const void* tmap, uint32_t bar_cluster_addr, void* smem_dst, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster_addr), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+DEVINL void tma_load_4d_pair(const void* tmap, uint32_t bar_cluster_addr, void* smem_dst, int x, int y, int z,
+                             int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster_addr), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 DEVINL void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {

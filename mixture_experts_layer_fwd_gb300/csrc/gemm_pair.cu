@@ -1,28 +1,44 @@
 // Grouped GEMM for bf16 operands on CTA pairs: one tcgen05 MMA spans the two
-// SMs of a cluster (cta_group::2), M = 256 rows x N = 256 columns per tile.
+// SMs of a cluster (cta_group::2).  The weights are the MMA's M side (256
+// weight rows per pair tile, 128 per SM) and the tokens its N side (up to 256
+// tokens per tile, any multiple of 16), so the accumulator holds C^T.
 //
-// Why pairs: a single SM that stages a 128 x 64 A tile and a 256 x 64 B tile
-// (48 KB) per k-step fits 4 stages in shared memory, and the time a stage
-// takes to come back (issue -> TMA from L2/HBM -> MMA -> free) is longer than
-// 4 stages of MMA work, so the tensor core waits.  With the pair each SM
-// stages its own 128 A rows and only half of B (32 KB per k-step) for the same
-// MMA work per SM, so 6 stages fit and the pipeline covers the round trip.
+// Why pairs: each SM stages its own 128 weight rows and only half of the
+// tile's tokens, so a 128-wide k step costs 64 KB of shared memory per SM for
+// an M=256 x N=256 MMA, and three such stages fit.
+//
+// Why weights on M: a group of r routed rows is cut into ceil(r/256) token
+// blocks of equal size rounded up to 16 (the MMA's N granularity), so a
+// group wastes at most 15 rows of MMA work per block instead of up to 255
+// rows of a 256-row M tile.
+//
+// Why 128-wide k stages with one copy per operand: every stage costs the
+// producer and the MMA issuer a fixed amount of barrier traffic (wait, arm,
+// commit) and every copy instruction adds issue time; two 64-wide k-blocks
+// per stage, each operand moved by one 3-D/4-D box (k-block as the outer
+// box dimension), halve that cost per MMA compared with 64-wide stages of two
+// 2-D copies.  Small-N tiles remain bound by that per-stage cost.
 //
 // Roles (both CTAs of the pair run the same tile sequence):
-//   warp 0      TMA producer of this CTA: A rows [tile_row + 128*rank, +128),
-//               B rows of this CTA's half of N; both loads complete on the
-//               leader CTA's full barrier (the leader arms it for both)
+//   warp 0      TMA producer of this CTA: one box of its 128 weight rows x
+//               2 k-blocks and one box of 128 token rows (from its half of
+//               the tile's tokens on) x 2 k-blocks; rows past the half are
+//               staged and not read by the MMA; both copies complete on the
+//               leader CTA's full barrier, which the leader arms for both
 //   warp 1      TMEM allocation of the pair; in the leader only, the MMA
-//               issuer: 4 x tcgen05.mma.cta_group::2 (M=256, N=256, K=16) per
-//               stage, commits multicast to both CTAs' empty / tfull barriers
-//   warps 2..5  epilogue: each CTA reads its own 128 accumulator rows from its
-//               tensor memory; SwiGLU / bf16 stores as the 1-SM kernel; then
-//               releases the accumulator on the leader's tempty barrier
-// For SwiGLU the leader stages the 128 gate rows of the tile and the peer the
-// matching 128 up rows, so accumulator columns [0,128) are gate, [128,256) up.
-// Tiles are (group, column block, 256-row block); a group's last row block
-// may extend past the group (rows of the next group or past the end): those
-// rows are computed and not stored.
+//               issuer: 8 x tcgen05.mma.cta_group::2 (M=256, N=tile tokens,
+//               K=16) per stage from precomputed descriptors, commits
+//               multicast to both CTAs' empty / tfull barriers
+//   warps 2..5  epilogue: each CTA reads its 128 accumulator lanes (weight
+//               rows) x tokens from its tensor memory and stores C[token, col]
+//               with 4-byte stores (two columns, exchanged between lanes);
+//               then releases the accumulator on the leader's tempty barrier
+// SwiGLU: each CTA stages the 64 gate rows of features [f0, f0+64) followed
+// by the 64 up rows of the same features (one 4-D TMA box), so accumulator
+// lanes 0..63 hold gate and 64..127 up.  The warp of gate lanes 32q and the
+// warp of up lanes 32q+64 swap half of their 32-token chunks through shared
+// memory (named barrier per warp pair) and each computes silu(gate) * up for
+// the chunks it stores.
 #include <cstring>
 
 #include "gemm_common.cuh"
@@ -31,37 +47,95 @@
 namespace moe {
 namespace gp {
 
-using gg::BM;
 using gg::MAX_G;
 using gg::Params;
 using gg::Prob;
-using gg::TileInfo;
 
-constexpr int TM = 2 * BM;            // rows per pair tile
-constexpr int BN = 256;               // accumulator columns (N of the MMA)
-constexpr int BK = 64;                // bf16 elements per k-step (128-byte rows)
-constexpr int A_TILE = BM * BK * 2;   // 16 KB: this CTA's 128 A rows
-constexpr int B_TILE = 128 * BK * 2;  // 16 KB: this CTA's half of B
-constexpr int STAGES = 6;
-constexpr int STAGE_BYTES = A_TILE + B_TILE;
+constexpr int TM = 256;               // most tokens per tile (N of the MMA)
+constexpr int WM = 128;               // weight rows per CTA (M of the MMA is 2 x WM)
+constexpr int BK = 64;                // bf16 elements per k-block (128-byte rows)
+constexpr int GU_ROWS = 64;           // SwiGLU: features per CTA (64 gate + 64 up rows)
+constexpr int A_TILE = WM * BK * 2;   // 16 KB: this CTA's weight rows
+constexpr int B_ROWS = 128;           // token rows staged per CTA (>= half of N)
+constexpr int B_TILE = B_ROWS * BK * 2;
+constexpr int KSUB = 2;               // k-blocks per pipeline stage (128 of K)
+constexpr int STAGES = 3;
+constexpr int STAGE_BYTES = KSUB * (A_TILE + B_TILE);  // [A k-block 0][A 1][B 0][B 1]
+constexpr uint32_t TX_BYTES_PAIR = 2 * STAGE_BYTES;    // both CTAs' loads, counted on the leader
 constexpr int NUM_WARPS = 6;
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int TMEM_COLS = 512;
-constexpr uint32_t TX_BYTES_PAIR = 2 * STAGE_BYTES;  // both CTAs' loads, counted on the leader
-constexpr int EXTRA = 2048 + 4 * (2 * MAX_G + 8);
-constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA;
+constexpr int EXTRA = (2048 + 4 * (2 * MAX_G + 8) + 15) & ~15;
+constexpr int XCH_FLOATS = 32 * 32;                // one 32-lane x 32-token chunk
+constexpr int XCH_BYTES = 2 * 2 * XCH_FLOATS * 4;  // 2 warp pairs x 2 directions
+constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA + XCH_BYTES + 64;
 static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
+static_assert(KSUB == 2, "the MMA issuer unrolls two k-blocks per stage");
 static_assert(SMEM <= 232448, "shared memory budget");
 
-template <int EPI>
 struct Tile {
-  static constexpr int N_OUT = (EPI == MOE_EPI_STORE_BF16) ? BN : BN / 2;  // output columns per tile
+  int pb;    // problem: 0 routed, 1 shared
+  int g;     // group inside the problem
+  int row0;  // first row of the tile's tokens in A / C
+  int cnt;   // tokens of the tile (1..256)
+  int n;     // MMA N: cnt rounded up to 16
+  int blk;   // weight block: 128 features (SwiGLU) or 256 output columns
 };
+
+// Tile t -> (group, weight block, token block), token blocks fastest so that
+// the pairs working at the same time share a weight block through L2.  A
+// group of `rows` rows has ceil(rows/256) token blocks of ng rows each (ng =
+// rows / blocks rounded up to 16); the last one takes the remainder.
+DEVINL Tile decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
+  int lo = 0, hi = GT;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  Tile ti;
+  const bool routed = lo < G;
+  ti.pb = routed ? 0 : 1;
+  ti.g = routed ? lo : 0;
+  const int start = routed ? s_off[lo] : 0;
+  const int rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
+  const int nb = (rows + TM - 1) / TM;
+  const int ng = ((rows + nb - 1) / nb + 15) & ~15;
+  const int local = t - s_prefix[lo];
+  ti.blk = local / nb;
+  const int m = local - ti.blk * nb;
+  ti.row0 = start + m * ng;
+  ti.cnt = min(ng, rows - m * ng);
+  ti.n = (ti.cnt + 15) & ~15;
+  return ti;
+}
+
+// Stores NV tokens x one column per lane as bf16: lanes 2j and 2j+1 hold
+// columns col_even and col_even+1 of the same tokens; after one exchange each
+// lane writes both columns of one token (even lane: tokens 2i, odd lane:
+// tokens 2i+1).  Tokens from valid_tokens on are not stored.
+template <int NV>
+DEVINL void store_pairs(const Prob& P, const float (&h)[NV], int col, int row_first, int valid_tokens, int lane) {
+  const bool odd = lane & 1;
+  const int col_even = col & ~1;
+  if (col_even >= P.n_out) return;  // uniform over the lanes sharing tokens: n_out % 32 == 0
+  uint16_t* C = static_cast<uint16_t*>(P.c);
+#pragma unroll
+  for (int j = 0; j < NV / 2; ++j) {
+    const float send = odd ? h[2 * j] : h[2 * j + 1];
+    const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+    const int t = 2 * j + (odd ? 1 : 0);
+    const float lo = odd ? recv : h[2 * j];
+    const float hi = odd ? h[2 * j + 1] : recv;
+    if (t < valid_tokens)
+      *reinterpret_cast<uint32_t*>(C + static_cast<size_t>(row_first + t) * P.n_out + col_even) =
+          pack_bf16x2(lo, hi);
+  }
+}
 
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __grid_constant__ Params p) {
   constexpr int S = STAGES;
-  constexpr int TN = Tile<EPI>::N_OUT;
+  constexpr bool SWIGLU = EPI == MOE_EPI_SWIGLU_BF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = base;
@@ -74,6 +148,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_prefix = reinterpret_cast<int*>(base + S * STAGE_BYTES + 256);
   int* s_off = s_prefix + MAX_G + 4;
+  float* xch = reinterpret_cast<float*>(base + S * STAGE_BYTES + EXTRA);
+  volatile int* pair_ok = reinterpret_cast<volatile int*>(xch + 4 * XCH_FLOATS);  // [2 pairs][gate, up]
   __shared__ int warp_sums[32];
 
   const int warp = threadIdx.x >> 5;
@@ -124,27 +200,32 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
       uint32_t phase = 0;
       bool ok = true;
       for (int t = cluster_id; t < total && ok; t += n_clusters) {
-        const TileInfo ti = gg::decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
         const Prob& P = p.prob[ti.pb];
         const void* ta = &p.tma_a[ti.pb];
         const void* tw = &p.tma_w[ti.pb];
-        const int a_y = ti.row0 + ti.m_blk * TM + static_cast<int>(rank) * BM;
-        const int w_base = ti.g * P.w_rows + ti.n_blk * TN;
-        // this CTA's half of B: STORE -> rows [128*rank, +128) of the 256-row
-        // block; SwiGLU -> the 128 gate rows (leader) or the 128 up rows (peer)
-        const int w_y = (EPI == MOE_EPI_STORE_BF16) ? w_base + static_cast<int>(rank) * 128
-                                                    : w_base + (leader ? 0 : P.n_out);
+        // this CTA's tokens start half of N into the tile (half <= 128)
+        const int b_y = ti.row0 + static_cast<int>(rank) * (ti.n >> 1);
+        // this CTA's 128 weight rows: SwiGLU -> gate and up rows of features
+        // [blk*128 + 64*rank, +64); STORE -> rows [blk*256 + 128*rank, +128)
+        const int f0 = ti.blk * 128 + static_cast<int>(rank) * GU_ROWS;
+        const int w_y0 = ti.g * P.w_rows + ti.blk * 256 + static_cast<int>(rank) * WM;
         const int nk = P.K / BK;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = 0; kb < nk; kb += KSUB) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, p.err, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* sb = stages + stage * STAGE_BYTES;
           const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
+          // one copy per operand moves both k-blocks of the stage (a k-block
+          // past the end of K is zero-filled and still counted)
           if (leader) mbar_arrive_expect_tx(&full[stage], TX_BYTES_PAIR);
-          tma_load_2d_pair(ta, fbar, sb, kb * BK, a_y);
-          tma_load_2d_pair(tw, fbar, sb + A_TILE, kb * BK, w_y);
+          if (SWIGLU)
+            tma_load_4d_pair(tw, fbar, sb, 0, f0, 2 * ti.g, kb);
+          else
+            tma_load_3d_pair(tw, fbar, sb, 0, w_y0, kb);
+          tma_load_3d_pair(ta, fbar, sb + KSUB * A_TILE, 0, b_y, kb);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -155,14 +236,19 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
   } else if (warp == 1) {
     // ===================================================== MMA issuer (leader)
     if (lane == 0 && leader) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(TM, BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
+      // The issuing thread's own instruction count per MMA sets the MMA
+      // rate for small N, so descriptors are built once: a stage, k-block
+      // and 16-wide k step only add (byte offset >> 4) to the start field.
+      const uint64_t a_desc0 = smem_desc_kmajor_sw128(smem_u32(stages));
+      const uint64_t b_desc0 = smem_desc_kmajor_sw128(smem_u32(stages + KSUB * A_TILE));
       for (int t = cluster_id; t < total && ok; t += n_clusters, ++it) {
-        const TileInfo ti = gg::decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
         const int nk = p.prob[ti.pb].K / BK;
+        const uint32_t idesc = idesc_bf16_f32(2 * WM, ti.n);
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         // both CTAs' epilogues must have drained this accumulator buffer
@@ -179,19 +265,25 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
           if (!ok) break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = 0; kb < nk; ++kb) {
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * TM);
+        for (int kb = 0; kb < nk; kb += KSUB) {
+          const int nsub = min(KSUB, nk - kb);
           if (!mbar_wait_bounded(&full[stage], phase, tmo, p.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + stage * STAGE_BYTES);
-          const uint32_t b_addr = a_addr + A_TILE;
+          const uint64_t da = a_desc0 + static_cast<uint64_t>((stage * STAGE_BYTES) >> 4);
+          const uint64_t db = b_desc0 + static_cast<uint64_t>((stage * STAGE_BYTES) >> 4);
+          const uint32_t acc0 = kb != 0 ? 1u : 0u;
+          umma_f16_pair(d, da, db, idesc, acc0);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_f16_pair(d, smem_desc_kmajor_sw128(a_addr + kk * 32), smem_desc_kmajor_sw128(b_addr + kk * 32),
-                          IDESC, (kb | kk) ? 1u : 0u);
+          for (int kk = 1; kk < BK / 16; ++kk) umma_f16_pair(d, da + 2 * kk, db + 2 * kk, idesc, 1u);
+          if (nsub > 1) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_f16_pair(d, da + (A_TILE >> 4) + 2 * kk, db + (B_TILE >> 4) + 2 * kk, idesc, 1u);
+          }
           umma_commit_pair_multicast(&empty[stage], 0x3);
           if (++stage == S) {
             stage = 0;
@@ -208,20 +300,75 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
   } else {
     // ===================================================== epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int r_in_tile = q * 32 + lane;
     const uint32_t tempty_leader = mapa_shared(smem_u32(&tempty[0]), 0);
+    // SwiGLU: quadrants 0,1 hold gate rows, 2,3 the up rows of the same
+    // features; warps (q, q+2) form exchange pair pi = q & 1
+    const int pi = q & 1;
+    const bool is_gate = q < 2;
+    float* x_to_up = xch + pi * 2 * XCH_FLOATS;  // gate values the up warp consumes
+    float* x_to_gate = x_to_up + XCH_FLOATS;     // up values the gate warp consumes
     int it = 0;
     for (int t = cluster_id; t < total; t += n_clusters, ++it) {
-      TileInfo ti = gg::decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
       const Prob& P = p.prob[ti.pb];
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
-      if (!mbar_wait_warp(&tfull[buf], use & 1u, tmo, p.err, abort_flag)) break;
+      bool ok = mbar_wait_warp(&tfull[buf], use & 1u, tmo, p.err, abort_flag);
+      if (SWIGLU) {
+        // both warps of the pair leave together if either wait gave up, so
+        // that neither is left alone at the exchange barriers below
+        if (lane == 0) pair_ok[pi * 2 + (is_gate ? 0 : 1)] = ok ? 1 : 0;
+        named_bar_sync(1 + pi, 64);
+        ok = pair_ok[pi * 2] && pair_ok[pi * 2 + 1];
+      }
+      if (!ok) break;
       tc_fence_after();
-      // this CTA holds rows [128*rank, +128) of the 256-row tile
-      ti.m_blk = 2 * ti.m_blk + static_cast<int>(rank);
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      gg::epilogue_tile<EPI, BN>(P, ti, taddr, r_in_tile, 1.0f);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * TM);
+      const int nch = (ti.cnt + 31) >> 5;
+      if (SWIGLU) {
+        const int col = ti.blk * 128 + static_cast<int>(rank) * GU_ROWS + pi * 32 + lane;  // feature
+        for (int c = 0; c < nch; c += 2) {
+          const bool has1 = c + 1 < nch;
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, v0);
+          if (has1) tmem_ld_32x32b_x32(taddr + (c + 1) * 32, v1);
+          tmem_ld_wait();
+          // the gate warp finishes chunk c, the up warp chunk c+1
+          if (is_gate) {
+            if (has1) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) x_to_up[j * 32 + lane] = __uint_as_float(v1[j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x_to_gate[j * 32 + lane] = __uint_as_float(v0[j]);
+          }
+          named_bar_sync(1 + pi, 64);
+          float h[32];
+          if (is_gate) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = gg::silu_f(__uint_as_float(v0[j])) * x_to_gate[j * 32 + lane];
+            store_pairs<32>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
+          } else if (has1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = gg::silu_f(x_to_up[j * 32 + lane]) * __uint_as_float(v1[j]);
+            store_pairs<32>(P, h, col, ti.row0 + (c + 1) * 32, ti.cnt - (c + 1) * 32, lane);
+          }
+          // the slots are rewritten by the next chunk pair
+          named_bar_sync(1 + pi, 64);
+        }
+      } else {
+        const int col = ti.blk * 256 + static_cast<int>(rank) * WM + q * 32 + lane;  // output column
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, v);
+          tmem_ld_wait();
+          float h[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) h[j] = __uint_as_float(v[j]);
+          store_pairs<32>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -287,7 +434,7 @@ static int launch(const Params& prm, cudaStream_t s) {
 
 static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
   Prob& q = prm.prob[slot];
-  const int tn = (epi == MOE_EPI_STORE_BF16) ? BN : BN / 2;
+  const int tn = (epi == MOE_EPI_STORE_BF16) ? 256 : 128;  // output columns per weight block
   q.n_out = P.N;
   q.K = P.K;
   q.w_rows = (epi == MOE_EPI_STORE_BF16) ? P.N : 2 * P.N;
@@ -298,8 +445,11 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
   q.c_sf = nullptr;
   q.a_g = q.w_g = q.c_g = nullptr;
   q.a_sf = q.w_sf = nullptr;
-  MOE_TRY(encode_tmap_2d(&prm.tma_a[slot], P.A, 2, P.K, static_cast<uint64_t>(P.a_rows), BK, BM, true));
-  MOE_TRY(encode_tmap_2d(&prm.tma_w[slot], P.W, 2, P.K, static_cast<uint64_t>(q.w_rows_total), BK, 128, true));
+  MOE_TRY(encode_tmap_kblocks(&prm.tma_a[slot], P.A, P.K, static_cast<uint64_t>(P.a_rows), B_ROWS, KSUB));
+  if (epi == MOE_EPI_STORE_BF16)
+    MOE_TRY(encode_tmap_kblocks(&prm.tma_w[slot], P.W, P.K, static_cast<uint64_t>(q.w_rows_total), WM, KSUB));
+  else
+    MOE_TRY(encode_tmap_gateup(&prm.tma_w[slot], P.W, P.K, P.N, P.groups, GU_ROWS, KSUB));
   return MOE_OK;
 }
 

@@ -249,6 +249,28 @@ def test_grouped_gemm_bf16(epi, N, K):
     assert err < 5e-3, err
 
 
+@pytest.mark.parametrize("epi", [0, 1])
+def test_grouped_gemm_bf16_token_blocks(epi):
+    """Groups that span several 256-token blocks, cut into equal blocks of a
+    multiple of 16 tokens (256, 257, 513, 1000 rows), next to tiny ones."""
+    m = api()
+    counts = [256, 257, 16, 513, 17, 1000, 2]
+    offs = _ragged_offsets(counts)
+    M, G, N, K = int(offs[-1]), len(counts), 256, 448
+    Wn = N if epi == 0 else 2 * N
+    g = torch.Generator().manual_seed(77 + epi)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(G, Wn, K, generator=g) * 0.05).to(torch.bfloat16)
+    C = m.moe_grouped_gemm(0, 0, epi, offs.to(DEV), N, K, A.to(DEV), W.to(DEV))
+    _sync()
+    ref = _gemm_ref(A.double().numpy(), W.double().numpy(), offs.numpy(), epi == 1, N)
+    err = oracle.rel_frobenius(C.float().cpu().numpy(), ref)
+    assert err < 5e-3, err
+    # every row is written: no row of C keeps the allocation's contents
+    row_err = np.abs(C.float().cpu().numpy() - ref).max(axis=1) / (np.abs(ref).max() + 1e-30)
+    assert row_err.max() < 2e-2, int(row_err.argmax())
+
+
 def test_grouped_gemm_nvfp4_weights():
     """bf16 A x NVFP4 W (codes + E4M3 scales + per-group fp32 scale)."""
     m = api()
