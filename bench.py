@@ -125,11 +125,12 @@ class ClockSampler:
 
 def gemm_traffic_per_launch():
     """DRAM bytes per grouped-GEMM launch at the bench workload, from the
-    committed ncu summary -- only while gemm.cu is the source it was taken on."""
+    committed ncu summary -- only while gemm_pair.cu is the source it was
+    taken on."""
     import hashlib
     import re
-    prof = os.path.join(ROOT, "profiles", "grouped_gemm_qwen3-235b-e32_T2048.md")
-    src = os.path.join(ROOT, "mixture_experts_layer_fwd_gb300", "csrc", "gemm.cu")
+    prof = os.path.join(ROOT, "profiles", "grouped_gemm_pair_qwen3-235b-e32_T2048.md")
+    src = os.path.join(ROOT, "mixture_experts_layer_fwd_gb300", "csrc", "gemm_pair.cu")
     try:
         text = open(prof).read()
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
@@ -206,6 +207,15 @@ def gemm_work(cfg, T, active_experts):
     return flops, weights + acts, weights
 
 
+def gemm_kernel_name(cfg):
+    """The grouped-GEMM kernel a layer's formats dispatch to."""
+    if cfg.w_fmt == "bf16" and cfg.act_fmt == "bf16":
+        return "grouped_gemm_pair_kernel"
+    if cfg.w_fmt == "nvfp4" and cfg.act_fmt == "nvfp4":
+        return "grouped_gemm_nvf4_kernel"
+    return "grouped_gemm_kernel"
+
+
 def tensor_peak(cfg, p):
     """Dense tensor peak of the MMA the path runs: bf16 (bf16 layers and the
     NVFP4-weight / bf16-activation layer, whose MMA is bf16), or NVFP4 (both
@@ -234,7 +244,7 @@ def roofline(cfg, T, gemm_ms, active, traffic, src):
              "frac": round(ach / p["hbm_gbs"], 4), "peak_source": f"hbm_gbs of {src} peaks",
              "algorithmic": f"{nbytes / 2 / 1e9:.3f} GB per launch ({wbytes / 1e9:.3f} GB of weights of "
                             f"{active} active experts per step)"}
-    r.update({"traffic": traffic, "kernel": "grouped_gemm_kernel (2 launches/step)", "mma": mma,
+    r.update({"traffic": traffic, "kernel": f"{gemm_kernel_name(cfg)} (2 launches/step)", "mma": mma,
               "t_roof_ms": round(max(t_tensor, t_hbm) * 1e3, 4)})
     return r
 

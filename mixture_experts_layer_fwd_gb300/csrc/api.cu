@@ -84,6 +84,28 @@ int encode_tmap_2d(CUtensorMap* m, const void* ptr, int elem_bytes, uint64_t inn
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
+// Any-rank tiled descriptor (rank <= 5): dims / box innermost first,
+// strides (bytes) of dims 1.. ; zero fill out of bounds.
+int encode_tmap_nd(CUtensorMap* m, const void* ptr, bool bf16, int rank, const uint64_t* dims,
+                   const uint64_t* strides, const uint32_t* box, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  if (rank < 1 || rank > 5) return MOE_ERR_INVALID_ARG;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                  static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 // bf16 [rows, K] viewed as [K/64 k-blocks][rows][64]: a box {64, box_rows,
 // kblocks} at (0, r, kb) stages k-blocks kb.. of rows r.. as consecutive
 // 128-byte-row tiles (one per k-block), 128-byte swizzle.

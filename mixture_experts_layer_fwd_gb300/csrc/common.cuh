@@ -24,6 +24,11 @@ unsigned int* device_error_word();  // device address of the error word (current
 // or 1-byte elements; zero fill out of bounds; optional 128-byte swizzle.
 int encode_tmap_2d(CUtensorMap* m, const void* ptr, int elem_bytes, uint64_t inner, uint64_t rows, uint32_t box_inner,
                    uint32_t box_rows, bool swizzle128);
+// Tiled TMA descriptor of any rank (<= 5) over bf16 or byte elements: dims
+// and box innermost first, strides in bytes for dims 1..rank-1 (they need
+// not increase: an outer box dimension may step along the inner one).
+int encode_tmap_nd(CUtensorMap* m, const void* ptr, bool bf16, int rank, const uint64_t* dims,
+                   const uint64_t* strides, const uint32_t* box, bool swizzle128);
 // bf16 [rows, K] (K % 64 == 0) as k-blocks of 64: a box at (0, r, kb)
 // stages `kblocks` consecutive 64-wide k-blocks of box_rows rows, each as its
 // own 128-byte-swizzled tile (zero fill past the end of K or the rows).
@@ -158,6 +163,20 @@ DEVINL void tma_load_2d(const void* tmap, uint64_t* bar, void* smem_dst, int x, 
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
           smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+DEVINL void tma_load_3d(const void* tmap, uint64_t* bar, void* smem_dst, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+DEVINL void tma_load_4d(const void* tmap, uint64_t* bar, void* smem_dst, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -329,6 +348,20 @@ DEVINL void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 32 consecutive 32-bit columns from registers: thread i of the
+// warp writes lane (base lane + i), columns [col, col+32).
+DEVINL void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major operand tile stored with the
 // 128-byte swizzle (rows of 128 bytes, 8-row groups 1024 bytes apart), as TMA

@@ -30,13 +30,12 @@ struct Prob {
 struct Params {
   CUtensorMap tma_a[2];  // [0] routed problem, [1] shared-expert problem
   CUtensorMap tma_w[2];
-  CUtensorMap tma_asf[2];  // scale rows of A / W (block-scaled kernel, when sf_tma)
+  CUtensorMap tma_asf[2];  // scale rows of A / W (512-element-stage FP4 kernel)
   CUtensorMap tma_wsf[2];
   Prob prob[2];
   const int32_t* offsets;  // [G+1] rows of each routed group in A
   int G;
   int shared_rows;  // rows of the shared problem; < 0: none
-  int sf_tma;       // block-scaled kernel: scale rows arrive by TMA (K % 256 == 0 everywhere)
   unsigned int* err;
   unsigned long long timeout_ns;
 };

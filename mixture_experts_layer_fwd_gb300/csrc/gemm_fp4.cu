@@ -7,13 +7,17 @@
 // activations are quantised to FP4 before dispatch, so both GEMM operands
 // arrive in NVFP4.
 //
+// This kernel serves the shapes the 512-element-stage kernel (gemm_fp4w.cu)
+// cannot: K % 256 != 0 or scale arrays not 16-byte aligned, where the scale
+// rows are not whole 16-byte slices and cannot travel by TMA.
+//
 // Design (one CTA per SM, warp-specialised), per pipeline stage of K = 256:
 //   warp 0      TMA: A tile 128 rows x 128 bytes (256 E2M1), B tile 128 rows x
 //               128 bytes, both with the 128-byte swizzle
-//   warp 6      scale loader: the E4M3 scales of the stage's A and B rows
-//               (row-major in global memory, 16 bytes per row per stage) are
-//               re-laid into four 512-byte blocks per operand, one per MMA of
-//               K = 64: row r's 4 scales go to byte 16*(r % 32) + 4*(r / 32)
+//   warp 6      scale loader: 4-byte asynchronous copies (cp.async) of the
+//               E4M3 scale words of the stage's A and B rows straight into
+//               four 512-byte blocks per operand, one per MMA of K = 64: row
+//               r's 4 scales go to byte 16*(r % 32) + 4*(r / 32)
 //   warp 1      MMA issuer: tcgen05.cp (32x128b, replicated to the four lane
 //               quadrants) moves each scale block into tensor memory, then 4
 //               block-scaled MMAs M=128 N=128 K=64 accumulate in fp32 in
@@ -42,15 +46,11 @@ constexpr int KE = 2 * ROW_BYTES;      // elements per stage
 constexpr int A_TILE = BM * ROW_BYTES; // 16 KB
 constexpr int B_TILE = BN * ROW_BYTES; // 16 KB
 constexpr int SF_TILE = 4 * 512;       // 4 scale blocks of 32 x 16 bytes
-constexpr int SF_RM = 128 * 16;        // one operand's scale rows as TMA lands them: 128 rows x 16 bytes
 constexpr int STAGES = 5;
-// per stage: A codes | B codes | A scale blocks | B scale blocks | A scale rows | B scale rows
-constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE + 2 * SF_RM;
+// per stage: A codes | B codes | A scale blocks | B scale blocks
+constexpr int STAGE_BYTES = A_TILE + B_TILE + 2 * SF_TILE;
 constexpr int OFF_SFA = A_TILE + B_TILE;
 constexpr int OFF_SFB = OFF_SFA + SF_TILE;
-constexpr int OFF_RMA = OFF_SFB + SF_TILE;
-constexpr int OFF_RMB = OFF_RMA + SF_RM;
-constexpr uint32_t SF_TX_BYTES = 2 * SF_RM;
 constexpr int NUM_WARPS = 7;
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int TMEM_COLS = 512;
@@ -171,16 +171,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4_kernel(const __g
             break;
           }
           uint8_t* sb = stages + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], TX_BYTES + (p.sf_tma ? SF_TX_BYTES : 0u));
+          mbar_arrive_expect_tx(&full[stage], TX_BYTES);
           tma_load_2d(ta, &full[stage], sb, kb * ROW_BYTES, a_y);
           tma_load_2d(tw, &full[stage], sb + A_TILE, kb * ROW_BYTES, w_y0);
           tma_load_2d(tw, &full[stage], sb + A_TILE + B_TILE / 2, kb * ROW_BYTES, w_y1);
-          if (p.sf_tma) {
-            // the stage's 16 scale bytes of every A and B row (4 words, one per MMA)
-            tma_load_2d(&p.tma_asf[ti.pb], &full[stage], sb + OFF_RMA, kb * 16, a_y);
-            tma_load_2d(&p.tma_wsf[ti.pb], &full[stage], sb + OFF_RMB, kb * 16, w_y0);
-            tma_load_2d(&p.tma_wsf[ti.pb], &full[stage], sb + OFF_RMB + SF_RM / 2, kb * 16, w_y1);
-          }
           issued[stage] += 1;
           if (++stage == S) {
             stage = 0;
@@ -198,41 +192,6 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4_kernel(const __g
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    if (p.sf_tma) {
-      // The scale rows arrived with the stage's TMA loads (row r's 16 bytes =
-      // its 4 scale words, one per MMA).  Re-lay them into the scale blocks:
-      // lane l moves rows l + 32 j; block kk's row l = {word kk of rows l,
-      // l+32, l+64, l+96}.  16-byte shared accesses, no bank conflicts.
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileInfo ti = gg::decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
-        const int nk = (p.prob[ti.pb].K + KE - 1) / KE;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_warp(&full[stage], phase, tmo, p.err, abort_flag)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sb = stages + stage * STAGE_BYTES;
-#pragma unroll
-          for (int op = 0; op < 2; ++op) {
-            const uint8_t* rm = sb + (op ? OFF_RMB : OFF_RMA);
-            uint8_t* blk = sb + (op ? OFF_SFB : OFF_SFA);
-            uint4 r[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) r[j] = *reinterpret_cast<const uint4*>(rm + (lane + 32 * j) * 16);
-            *reinterpret_cast<uint4*>(blk + 0 * 512 + lane * 16) = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);
-            *reinterpret_cast<uint4*>(blk + 1 * 512 + lane * 16) = make_uint4(r[0].y, r[1].y, r[2].y, r[3].y);
-            *reinterpret_cast<uint4*>(blk + 2 * 512 + lane * 16) = make_uint4(r[0].z, r[1].z, r[2].z, r[3].z);
-            *reinterpret_cast<uint4*>(blk + 3 * 512 + lane * 16) = make_uint4(r[0].w, r[1].w, r[2].w, r[3].w);
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(&sf_full[stage]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    } else {
     // Scale rows not 16-byte aligned (K % 256 != 0): per-word asynchronous
     // copies; a stage is signalled SF_LAG stages after its copies were issued
     // (after they completed and were fenced for the tensor cores' async
@@ -281,7 +240,6 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4_kernel(const __g
     cp_async_wait_group<0>();
     fence_proxy_async_smem();
     for (int i = (issued > SF_LAG ? issued - SF_LAG : 0); i < issued; ++i) mbar_arrive(&sf_full[i % S]);
-    }
   } else if (warp == 1) {
     // ===================================================== MMA issuer
     if (lane == 0) {
@@ -382,7 +340,7 @@ static int launch(const Params& prm, cudaStream_t s) {
   return check_launch();
 }
 
-static int fill(Params& prm, int slot, int epi, const GemmProblem& P, bool sf_tma) {
+static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
   Prob& q = prm.prob[slot];
   const int tn = (epi == MOE_EPI_STORE_BF16) ? BN : BN / 2;
   q.n_out = P.N;
@@ -401,12 +359,6 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P, bool sf_tm
   MOE_TRY(encode_tmap_2d(&prm.tma_a[slot], P.A, 1, P.K / 2, static_cast<uint64_t>(P.a_rows), ROW_BYTES, BM, true));
   MOE_TRY(encode_tmap_2d(&prm.tma_w[slot], P.W, 1, P.K / 2, static_cast<uint64_t>(q.w_rows_total), ROW_BYTES,
                          BN / 2, true));
-  if (sf_tma) {
-    // scale rows: K/16 bytes per row, 16 bytes (one stage) per box row
-    MOE_TRY(encode_tmap_2d(&prm.tma_asf[slot], P.A_sf, 1, P.K / 16, static_cast<uint64_t>(P.a_rows), 16, BM, false));
-    MOE_TRY(encode_tmap_2d(&prm.tma_wsf[slot], P.W_sf, 1, P.K / 16, static_cast<uint64_t>(q.w_rows_total), 16,
-                           BN / 2, false));
-  }
   return MOE_OK;
 }
 
@@ -423,13 +375,13 @@ int grouped_gemm_launch_nvf4(int epi, const GemmProblem& routed, const int32_t* 
   // 16-byte stage slices (K % 256 == 0) and the scale arrays are 16-byte aligned
   const bool sf_tma = routed.K % 256 == 0 && aligned(routed.A_sf, 16) && aligned(routed.W_sf, 16) &&
                       (!have_shared || (sh->K % 256 == 0 && aligned(sh->A_sf, 16) && aligned(sh->W_sf, 16)));
-  prm.sf_tma = sf_tma ? 1 : 0;
-  MOE_TRY(gg4::fill(prm, 0, epi, routed, sf_tma));
+  if (sf_tma) return grouped_gemm_launch_nvf4_wide(epi, routed, offsets, G, sh, shared_rows, s);
+  MOE_TRY(gg4::fill(prm, 0, epi, routed));
   prm.offsets = offsets;
   prm.G = G;
   prm.shared_rows = -1;
   if (have_shared) {
-    MOE_TRY(gg4::fill(prm, 1, epi, *sh, sf_tma));
+    MOE_TRY(gg4::fill(prm, 1, epi, *sh));
     prm.shared_rows = shared_rows;
   }
   prm.err = device_error_word();

@@ -41,8 +41,12 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
 int grouped_gemm_launch_pair(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                              const GemmProblem* sh, int shared_rows, cudaStream_t s);
 
-// Both operands NVFP4: block-scaled FP4 tensor-core kernel (gemm_fp4.cu).
+// Both operands NVFP4: block-scaled FP4 tensor-core kernels; dispatches to
+// the 512-element-stage kernel (gemm_fp4w.cu) when K % 256 == 0 and the
+// scale arrays are 16-byte aligned, else to gemm_fp4.cu's kernel.
 int grouped_gemm_launch_nvf4(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                              const GemmProblem* sh, int shared_rows, cudaStream_t s);
+int grouped_gemm_launch_nvf4_wide(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
+                                  const GemmProblem* sh, int shared_rows, cudaStream_t s);
 
 }  // namespace moe
