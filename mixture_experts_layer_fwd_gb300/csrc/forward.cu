@@ -151,18 +151,26 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
   MOE_TRY(mark(events, 1, s));
   if (a4) MOE_TRY(quant_launch(x, 1, T, H, nullptr, b.xq, b.xsf, b.gx, b.qws, quant_ws_bytes(1), s));
   MOE_TRY(mark(events, 2, s));
+  // NVFP4 weights with bf16 activations: when the tensor-memory kernel takes
+  // all four problems (every K a multiple of 256, 16-byte aligned weight
+  // scales), x is permuted into fp16 once and h is kept in fp16, the inputs
+  // of that kernel's fp16 MMA
+  const bool w4 = L->w_fmt == MOE_FMT_NVFP4;
+  const bool f16 = w4 && !a4 && H % 256 == 0 && L->I % 256 == 0 && aligned(L->w13_sf, 16) &&
+                   aligned(L->w2_sf, 16) &&
+                   (L->I_s == 0 || (L->I_s % 256 == 0 && aligned(L->ws13_sf, 16) && aligned(L->ws2_sf, 16)));
   if (a4)
     MOE_TRY(permute_launch(b.idx, T, k, E, b.xq, H / 2, b.xsf, H / 16, b.counts, b.offsets, b.row_of, b.src_tok, b.xp,
                            b.xp_sf, b.perm_ws, b.perm_ws_bytes, s));
   else
     MOE_TRY(permute_launch(b.idx, T, k, E, x, H * 2, nullptr, 0, b.counts, b.offsets, b.row_of, b.src_tok, b.xp,
-                           nullptr, b.perm_ws, b.perm_ws_bytes, s));
+                           nullptr, b.perm_ws, b.perm_ws_bytes, s, f16));
 
   MOE_TRY(mark(events, 3, s));
 
   // gate/up projection + SwiGLU (routed groups + shared expert)
-  const int epi1 = a4 ? MOE_EPI_SWIGLU_NVFP4 : MOE_EPI_SWIGLU_BF16;
-  GemmProblem r1{b.xp, b.xp_sf, b.gx, Tk, L->w13, L->w13_sf, L->w13_g, E, b.h, b.h_sf, L->g_h, L->I, H};
+  const int epi1 = a4 ? MOE_EPI_SWIGLU_NVFP4 : (f16 ? kEpiSwigluF16 : MOE_EPI_SWIGLU_BF16);
+  GemmProblem r1{b.xp, b.xp_sf, b.gx, Tk, L->w13, L->w13_sf, L->w13_g, E, b.h, b.h_sf, L->g_h, L->I, H, f16};
   GemmProblem s1{a4 ? static_cast<const void*>(b.xq) : static_cast<const void*>(x),
                  b.xsf, b.gx, T, L->ws13, L->ws13_sf, L->ws13_g, 1, b.hs, b.hs_sf, L->g_hs, L->I_s, H};
   MOE_TRY(grouped_gemm_launch(epi1, L->act_fmt, L->w_fmt, r1, b.offsets, E, L->I_s ? &s1 : nullptr, T, s));
@@ -170,8 +178,8 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
   MOE_TRY(mark(events, 4, s));
 
   // down projection
-  GemmProblem r2{b.h, b.h_sf, L->g_h, Tk, L->w2, L->w2_sf, L->w2_g, E, b.Y, nullptr, nullptr, H, L->I};
-  GemmProblem s2{b.hs, b.hs_sf, L->g_hs, T, L->ws2, L->ws2_sf, L->ws2_g, 1, b.Ys, nullptr, nullptr, H, L->I_s};
+  GemmProblem r2{b.h, b.h_sf, L->g_h, Tk, L->w2, L->w2_sf, L->w2_g, E, b.Y, nullptr, nullptr, H, L->I, f16};
+  GemmProblem s2{b.hs, b.hs_sf, L->g_hs, T, L->ws2, L->ws2_sf, L->ws2_g, 1, b.Ys, nullptr, nullptr, H, L->I_s, f16};
   MOE_TRY(grouped_gemm_launch(MOE_EPI_STORE_BF16, L->act_fmt, L->w_fmt, r2, b.offsets, E, L->I_s ? &s2 : nullptr, T,
                               s));
 

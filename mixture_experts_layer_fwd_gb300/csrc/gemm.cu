@@ -424,6 +424,7 @@ static int check_problem(int epi, bool a4, bool w4, const GemmProblem& P) {
   if (a4 && (!P.A_sf || !P.A_g || !aligned(P.A_sf, 4))) return MOE_ERR_INVALID_ARG;
   if (w4 && (!P.W_sf || !P.W_g || !aligned(P.W_sf, 4))) return MOE_ERR_INVALID_ARG;
   if (epi == MOE_EPI_SWIGLU_NVFP4 && (!P.C_sf || !P.c_g || !aligned(P.C_sf, 2))) return MOE_ERR_INVALID_ARG;
+  if (P.a_f16 && (a4 || !w4)) return MOE_ERR_UNSUPPORTED;
   const long long w_rows = static_cast<long long>(P.groups) * ((epi == MOE_EPI_STORE_BF16) ? P.N : 2 * P.N);
   if (w_rows >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -436,8 +437,9 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
                         const GemmProblem* sh, int shared_rows, cudaStream_t s) {
   const bool a4 = a_fmt == MOE_FMT_NVFP4, w4 = w_fmt == MOE_FMT_NVFP4;
   if (G < 1 || G > gg::MAX_G - 1 || !offsets) return MOE_ERR_INVALID_ARG;
-  if (epi < MOE_EPI_STORE_BF16 || epi > MOE_EPI_SWIGLU_NVFP4) return MOE_ERR_INVALID_ARG;
+  if ((epi < MOE_EPI_STORE_BF16 || epi > MOE_EPI_SWIGLU_NVFP4) && epi != kEpiSwigluF16) return MOE_ERR_INVALID_ARG;
   if (a4 && !w4) return MOE_ERR_UNSUPPORTED;
+  if (epi == kEpiSwigluF16 && (a4 || !w4)) return MOE_ERR_UNSUPPORTED;
   if (epi == MOE_EPI_SWIGLU_NVFP4 && !(a4 && w4)) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_problem(epi, a4, w4, routed));
   if (sh) MOE_TRY(check_problem(epi, a4, w4, *sh));
@@ -447,6 +449,13 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
   if (a4 && w4) return grouped_gemm_launch_nvf4(epi, routed, offsets, G, sh, shared_rows, s);
   if (!a4 && !w4) return grouped_gemm_launch_pair(epi, routed, offsets, G, sh, shared_rows, s);
   const bool have_shared = sh != nullptr && shared_rows > 0;
+  // bf16 x NVFP4 weights: the tensor-memory kernel when the weight scale rows
+  // are whole 16-byte slices per 256-element stage; fp16 inputs and the fp16
+  // epilogue exist only there
+  if (routed.K % 256 == 0 && aligned(routed.W_sf, 16) &&
+      (!have_shared || (sh->K % 256 == 0 && aligned(sh->W_sf, 16))))
+    return grouped_gemm_launch_w4a16(epi, routed, offsets, G, sh, shared_rows, s);
+  if (epi == kEpiSwigluF16 || routed.a_f16 || (have_shared && sh->a_f16)) return MOE_ERR_UNSUPPORTED;
   gg::Params prm;
   memset(&prm, 0, sizeof(prm));
   MOE_TRY(fill_prob(prm, 0, epi, a4, w4, routed));
@@ -479,6 +488,7 @@ extern "C" int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue, int G, const
                                 const uint8_t* W_sf, const float* W_g, void* C, uint8_t* C_sf, const float* c_g,
                                 void* stream) {
   if (M_total < 0) return MOE_ERR_INVALID_ARG;
+  if (epilogue < MOE_EPI_STORE_BF16 || epilogue > MOE_EPI_SWIGLU_NVFP4) return MOE_ERR_INVALID_ARG;
   if (M_total == 0) return MOE_OK;
   GemmProblem P{A, A_sf, A_g, M_total, W, W_sf, W_g, G, C, C_sf, c_g, N, K};
   return grouped_gemm_launch(epilogue, a_fmt, w_fmt, P, offsets, G, nullptr, 0, static_cast<cudaStream_t>(stream));

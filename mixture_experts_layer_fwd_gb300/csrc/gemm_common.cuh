@@ -25,6 +25,7 @@ struct Prob {
   const float* c_g;
   const uint8_t* a_sf;
   const uint8_t* w_sf;
+  int a_f16;         // A holds fp16 (else bf16), NVFP4-weight kernel
 };
 
 struct Params {

@@ -1,0 +1,563 @@
+// Grouped GEMM for NVFP4 weights x bf16 activations (W4A16).
+//
+// "Driving vLLM WideEP ... (Part I)", section "NVFP4 GEMM for MoE and
+// O-proj": packed 4-bit weights with per-group FP8 scales, dequantised on
+// the fly.  There is no tensor-core MMA that takes FP4 and bf16 operands
+// together, so the weights are expanded to 16-bit on the SM: cvt e2m1x2 ->
+// fp16x2 (one instruction per two values) times the E4M3 block scale (exact:
+// e2m1 * e4m3 has at most five significant bits and lies in fp16's normal
+// range), and the MMA runs kind::f16 in fp16.  Tokens given in bf16 are
+// converted to fp16 in shared memory per stage (exact for |x| in [2^-14,
+// 65504], saturating beyond); inside the layer forward they arrive in fp16
+// already (the permutation converts x once, the gate/up epilogue stores h
+// as fp16), which spares re-converting a token block for every weight tile.
+//
+// Why the expanded weights go to tensor memory: written to shared memory
+// they would cost 2 bytes per weight on the way in and 2 on the way out to
+// the MMA, which caps the weight stream near 0.6 of HBM bandwidth; the MMA
+// can read its A operand from tensor memory instead (tcgen05.mma [a-tmem]).
+//
+// Tiles: weights on the MMA's M side (128 weight rows), tokens on N (a group
+// of r routed rows is cut into ceil(r/64) equal token blocks rounded up to
+// 16; N <= 64), so a weight tile is expanded once per 64 tokens and a decode
+// step (a few tokens per expert) streams each weight once.
+//
+// Roles (one CTA per SM):
+//   warp 0       TMA producer, per 256-element k stage: the tile's packed
+//                codes (128 rows x 128 bytes, 128-byte swizzle; SwiGLU: 64
+//                gate rows then the 64 up rows of the same features), their
+//                scales (128 rows x 16 bytes), and the tokens (4 k-blocks x
+//                16 or 64 rows x 128 bytes, 128-byte swizzle)
+//   warps 6..13  converters, two per TMEM lane quadrant (one per half of
+//                the stage's K): the tokens bf16 -> fp16 in place, and each
+//                thread's weight row (its TMEM lane) e2m1 x e4m3 -> fp16 into
+//                one of three 128-column slots of tensor memory (tcgen05.st)
+//   warp 1       TMEM allocation; MMA issuer: 16 x tcgen05.mma kind::f16
+//                M=128 N<=64 K=16 per stage, A from the slot, B (tokens) from
+//                shared memory, into one of two 64-column accumulators
+//   warps 2..5   epilogue: accumulator lanes (weight rows) x tokens, scaled
+//                by the weights' fp32 global scale; SwiGLU pairs gate lanes
+//                32q with up lanes 32q+64 through shared memory; 4-byte bf16
+//                stores of C[token, col]
+// Requires K % 256 == 0 and 16-byte aligned scale arrays; other shapes take
+// the converter kernel of gemm.cu.
+#include <cstring>
+
+#include "gemm_common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace gw4 {
+
+using gg::MAX_G;
+using gg::Params;
+using gg::Prob;
+
+constexpr int WM = 128;                   // weight rows per tile (M of the MMA)
+constexpr int TM = 64;                    // most tokens per tile (N of the MMA)
+constexpr int SMALL_N = 16;               // tiles of <= 16 tokens stage 16 token rows
+constexpr int KS = 256;                   // elements per stage
+constexpr int CODE_TILE = WM * KS / 2;    // 16 KB of packed E2M1
+constexpr int SF_TILE = WM * KS / 16;     // 2 KB: 16 scale bytes per row
+constexpr int TOK_KBLK = KS / 64;         // 64-element k-blocks of tokens per stage
+constexpr int TOK_TILE = TM * KS * 2;     // 32 KB: up to 64 token rows
+constexpr int OFF_SF = CODE_TILE;
+constexpr int OFF_TOK = CODE_TILE + SF_TILE;
+constexpr int STAGE_BYTES = OFF_TOK + TOK_TILE;
+constexpr int STAGES = 4;
+constexpr int ASLOTS = 3;                 // expanded-weight slots in tensor memory
+constexpr int ACC_COLS = TM;              // accumulator columns per buffer
+constexpr int A_COLS = KS / 2;            // fp16 pairs per row per stage
+constexpr int A_COL0 = 2 * ACC_COLS;
+constexpr int TMEM_COLS = 512;
+constexpr int CONV_WARPS = 8;
+constexpr int CONV_THREADS = CONV_WARPS * 32;
+constexpr int NUM_WARPS = 6 + CONV_WARPS;
+constexpr int THREADS = NUM_WARPS * 32;
+constexpr int XCH_FLOATS = 32 * 32;
+constexpr int XCH_BYTES = 2 * 2 * XCH_FLOATS * 4;
+constexpr int EXTRA = (256 + 4 * 2 * (MAX_G + 4) + 15) & ~15;
+constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA + XCH_BYTES + 64;
+static_assert(OFF_TOK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(A_COL0 + ASLOTS * A_COLS <= TMEM_COLS, "tensor memory budget");
+static_assert(SMEM <= 232448, "shared memory budget");
+
+struct Tile {
+  int pb, g, row0, cnt, n, blk;
+};
+
+// As the bf16 pair kernel's schedule, with token blocks of at most TM rows.
+DEVINL Tile decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
+  int lo = 0, hi = GT;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  Tile ti;
+  const bool routed = lo < G;
+  ti.pb = routed ? 0 : 1;
+  ti.g = routed ? lo : 0;
+  const int start = routed ? s_off[lo] : 0;
+  const int rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
+  const int nb = (rows + TM - 1) / TM;
+  const int ng = ((rows + nb - 1) / nb + 15) & ~15;
+  const int local = t - s_prefix[lo];
+  ti.blk = local / nb;
+  const int m = local - ti.blk * nb;
+  ti.row0 = start + m * ng;
+  ti.cnt = min(ng, rows - m * ng);
+  ti.n = (ti.cnt + 15) & ~15;
+  return ti;
+}
+
+DEVINL uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
+  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+DEVINL uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+DEVINL uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Stores NV tokens x one column per lane as bf16, or fp16 when F16 (see
+// gemm_pair.cu).
+template <int NV, bool F16>
+DEVINL void store_pairs(const Prob& P, const float (&h)[NV], int col, int row_first, int valid_tokens, int lane) {
+  const bool odd = lane & 1;
+  const int col_even = col & ~1;
+  if (col_even >= P.n_out) return;
+  uint16_t* C = static_cast<uint16_t*>(P.c);
+#pragma unroll
+  for (int j = 0; j < NV / 2; ++j) {
+    const float send = odd ? h[2 * j] : h[2 * j + 1];
+    const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+    const int t = 2 * j + (odd ? 1 : 0);
+    const float lo = odd ? recv : h[2 * j];
+    const float hi = odd ? h[2 * j + 1] : recv;
+    if (t < valid_tokens)
+      *reinterpret_cast<uint32_t*>(C + static_cast<size_t>(row_first + t) * P.n_out + col_even) =
+          F16 ? pack_f16x2_sat(lo, hi) : pack_bf16x2(lo, hi);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __grid_constant__ Params p) {
+  constexpr int S = STAGES;
+  constexpr bool SWIGLU = EPI != MOE_EPI_STORE_BF16;
+  constexpr bool OUT_F16 = EPI == kEpiSwigluF16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = base;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + S * STAGE_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* afull = empty + S;
+  uint64_t* aempty = afull + ASLOTS;
+  uint64_t* tfull = aempty + ASLOTS;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_prefix = reinterpret_cast<int*>(base + S * STAGE_BYTES + 256);
+  int* s_off = s_prefix + MAX_G + 4;
+  float* xch = reinterpret_cast<float*>(base + S * STAGE_BYTES + EXTRA);
+  volatile int* pair_ok = reinterpret_cast<volatile int*>(xch + 4 * XCH_FLOATS);
+  __shared__ int warp_sums[32];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.G;
+  const int GT = G + (p.shared_rows >= 0 ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < ASLOTS; ++a) {
+      mbar_init(&afull[a], CONV_WARPS);
+      mbar_init(&aempty[a], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);  // the 4 epilogue warps
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  gg::build_schedule<THREADS, NUM_WARPS, TM>(p, s_off, s_prefix, warp_sums);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = s_prefix[GT];
+  const unsigned long long tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    // tma_w: packed codes, tma_wsf: weight scales, tma_a / tma_asf: tokens
+    // with 64-row / 16-row boxes
+    if (lane == 0) {
+      for (int pb = 0; pb < (p.shared_rows >= 0 ? 2 : 1); ++pb) {
+        tma_prefetch_desc(&p.tma_a[pb]);
+        tma_prefetch_desc(&p.tma_asf[pb]);
+        tma_prefetch_desc(&p.tma_w[pb]);
+        tma_prefetch_desc(&p.tma_wsf[pb]);
+      }
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[S];
+#pragma unroll
+      for (int s = 0; s < S; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const Prob& P = p.prob[ti.pb];
+        const bool small = ti.n <= SMALL_N;
+        const void* tt = small ? &p.tma_asf[ti.pb] : &p.tma_a[ti.pb];
+        const uint32_t tx = static_cast<uint32_t>(CODE_TILE + SF_TILE + TOK_KBLK * (small ? SMALL_N : TM) * 128);
+        const int f0 = ti.blk * (WM / 2);                  // SwiGLU: 64 features
+        const int w_y = ti.g * P.w_rows + ti.blk * WM;     // STORE: 128 weight rows
+        const int nk = P.K / KS;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sb = stages + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], tx);
+          if (SWIGLU) {
+            tma_load_3d(&p.tma_w[ti.pb], &full[stage], sb, kb * (KS / 2), f0, 2 * ti.g);
+            tma_load_3d(&p.tma_wsf[ti.pb], &full[stage], sb + OFF_SF, kb * (KS / 16), f0, 2 * ti.g);
+          } else {
+            tma_load_2d(&p.tma_w[ti.pb], &full[stage], sb, kb * (KS / 2), w_y);
+            tma_load_2d(&p.tma_wsf[ti.pb], &full[stage], sb + OFF_SF, kb * (KS / 16), w_y);
+          }
+          tma_load_3d(tt, &full[stage], sb + OFF_TOK, 0, ti.row0, kb * TOK_KBLK);
+          issued[stage] += 1;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < S; ++s)
+          if (issued[s]) mbar_wait_bounded(&full[s], (issued[s] - 1u) & 1u, 1000000000ull, p.err, nullptr);
+      }
+    }
+  } else if (warp >= 6) {
+    // ===================================================== converters
+    const int cw = warp - 6;
+    const int ctid = cw * 32 + lane;
+    const int q = warp & 3;          // TMEM lane quadrant
+    const int kh = cw >> 2;          // half of the stage's K this warp expands
+    const int row = q * 32 + lane;   // weight row of the tile = TMEM lane
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const int nk = p.prob[ti.pb].K / KS;
+      const int kstride = (ti.n <= SMALL_N ? SMALL_N : TM) * 128;
+      // 16-byte chunks of the token rows the MMA reads, when given in bf16
+      const int tok_chunks = p.prob[ti.pb].a_f16 ? 0 : TOK_KBLK * ti.n * 8;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_warp(&full[stage], phase, tmo, p.err, abort_flag) ||
+            !mbar_wait_warp(&aempty[slot], sphase ^ 1u, tmo, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sb = stages + stage * STAGE_BYTES;
+        // tokens: bf16 -> fp16 in place (the swizzle moves whole 16-byte chunks)
+        for (int c = ctid; c < tok_chunks; c += CONV_THREADS) {
+          const int kblk = c / (ti.n * 8);
+          const int rem = c - kblk * ti.n * 8;
+          uint4* ptr = reinterpret_cast<uint4*>(sb + OFF_TOK + kblk * kstride + rem * 16);
+          uint4 v = *ptr;
+          v.x = bf16x2_to_f16x2_sat(v.x);
+          v.y = bf16x2_to_f16x2_sat(v.y);
+          v.z = bf16x2_to_f16x2_sat(v.z);
+          v.w = bf16x2_to_f16x2_sat(v.w);
+          *ptr = v;
+        }
+        // weights: this thread's row, elements [kh*128, +128) of the stage
+        const uint8_t* crow = sb + row * 128;
+        const uint2 sw = *reinterpret_cast<const uint2*>(sb + OFF_SF + row * 16 + kh * 8);
+        uint32_t r[64];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int j = 4 * kh + c4;  // 16-byte chunk of the row (32 elements, two scale blocks)
+          const uint4 cv = *reinterpret_cast<const uint4*>(crow + ((j ^ (row & 7)) << 4));
+          const uint32_t sbytes = ((c4 < 2 ? sw.x : sw.y) >> (16 * (c4 & 1))) & 0xFFFFu;
+          const uint32_t s2 = e4m3x2_to_f16x2(sbytes);
+          const uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
+          const uint32_t words[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) {
+            const uint32_t sc = wi < 2 ? s_lo : s_hi;
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi)
+              r[c4 * 16 + wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xFFu), sc);
+          }
+        }
+        tmem_st_32x32b_x64(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(A_COL0 + slot * A_COLS + kh * 64),
+                           r);
+        tmem_st_wait();
+        fence_proxy_async_smem();  // the converted tokens are read by the MMA (async proxy)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[slot]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++slot == ASLOTS) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, sphase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const int nk = p.prob[ti.pb].K / KS;
+        const uint32_t idesc = idesc_f16_f32(WM, ti.n);
+        const uint32_t kstride = static_cast<uint32_t>((ti.n <= SMALL_N ? SMALL_N : TM) * 128);
+        const int buf = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        if (!mbar_wait_bounded(&tempty[buf], (use & 1u) ^ 1u, tmo, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * ACC_COLS);
+        for (int kb = 0; kb < nk; ++kb) {
+          // the converters saw the stage land (full) before they filled the slot
+          if (!mbar_wait_bounded(&afull[slot], sphase, tmo, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tok = smem_u32(stages + stage * STAGE_BYTES + OFF_TOK);
+          const uint32_t a0 = tmem_base + static_cast<uint32_t>(A_COL0 + slot * A_COLS);
+#pragma unroll
+          for (int kk = 0; kk < KS / 16; ++kk)
+            umma_f16_ts(d, a0 + 8 * kk, smem_desc_kmajor_sw128(tok + (kk >> 2) * kstride + (kk & 3) * 32), idesc,
+                        (kb | kk) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          umma_commit(&aempty[slot]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++slot == ASLOTS) {
+            slot = 0;
+            sphase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(&tfull[buf]);
+      }
+      if (!ok) {
+        umma_commit(drain);
+        mbar_wait_bounded(drain, 0, 1000000000ull, p.err, nullptr);
+      }
+    }
+  } else {
+    // ===================================================== epilogue (warps 2..5)
+    const int q = warp & 3;
+    const int pi = q & 1;
+    const bool is_gate = q < 2;
+    float* x_to_up = xch + pi * 2 * XCH_FLOATS;
+    float* x_to_gate = x_to_up + XCH_FLOATS;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const Prob& P = p.prob[ti.pb];
+      const int buf = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      bool ok = mbar_wait_warp(&tfull[buf], use & 1u, tmo, p.err, abort_flag);
+      if (SWIGLU) {
+        // both warps of the exchange pair leave together if either gave up
+        if (lane == 0) pair_ok[pi * 2 + (is_gate ? 0 : 1)] = ok ? 1 : 0;
+        named_bar_sync(1 + pi, 64);
+        ok = pair_ok[pi * 2] && pair_ok[pi * 2 + 1];
+      }
+      if (!ok) break;
+      tc_fence_after();
+      const float scale = __ldg(P.w_g + ti.g);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * ACC_COLS);
+      const int nch = (ti.cnt + 31) >> 5;
+      if (SWIGLU) {
+        const int col = ti.blk * (WM / 2) + pi * 32 + lane;  // feature
+        for (int c = 0; c < nch; c += 2) {
+          const bool has1 = c + 1 < nch;
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, v0);
+          if (has1) tmem_ld_32x32b_x32(taddr + (c + 1) * 32, v1);
+          tmem_ld_wait();
+          if (is_gate) {
+            if (has1) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) x_to_up[j * 32 + lane] = __uint_as_float(v1[j]) * scale;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x_to_gate[j * 32 + lane] = __uint_as_float(v0[j]) * scale;
+          }
+          named_bar_sync(1 + pi, 64);
+          float h[32];
+          if (is_gate) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              h[j] = gg::silu_f(__uint_as_float(v0[j]) * scale) * x_to_gate[j * 32 + lane];
+            store_pairs<32, OUT_F16>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
+          } else if (has1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              h[j] = gg::silu_f(x_to_up[j * 32 + lane]) * (__uint_as_float(v1[j]) * scale);
+            store_pairs<32, OUT_F16>(P, h, col, ti.row0 + (c + 1) * 32, ti.cnt - (c + 1) * 32, lane);
+          }
+          named_bar_sync(1 + pi, 64);
+        }
+      } else {
+        const int col = ti.blk * WM + q * 32 + lane;  // output column
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, v);
+          tmem_ld_wait();
+          float h[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) h[j] = __uint_as_float(v[j]) * scale;
+          store_pairs<32, false>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // a wait ran out: give copies and MMAs already in flight time to land
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+static int launch(const Params& prm, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(grouped_gemm_w4a16_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) {
+      set_cuda_error(e);
+      return MOE_ERR_CUDA;
+    }
+    attr_done[dev] = true;
+  }
+  grouped_gemm_w4a16_kernel<EPI><<<num_sms(), THREADS, SMEM, s>>>(prm);
+  return check_launch();
+}
+
+static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
+  Prob& q = prm.prob[slot];
+  const bool swiglu = epi != MOE_EPI_STORE_BF16;
+  const int tn = swiglu ? WM / 2 : WM;  // output columns per weight tile
+  q.n_out = P.N;
+  q.K = P.K;
+  q.w_rows = swiglu ? 2 * P.N : P.N;
+  q.n_tiles = (P.N + tn - 1) / tn;
+  q.a_rows = P.a_rows;
+  q.w_rows_total = P.groups * q.w_rows;
+  q.c = P.C;
+  q.c_sf = nullptr;
+  q.a_g = nullptr;
+  q.w_g = P.W_g;
+  q.c_g = nullptr;
+  q.a_sf = nullptr;
+  q.w_sf = P.W_sf;
+  q.a_f16 = P.a_f16 ? 1 : 0;
+  const uint64_t K = static_cast<uint64_t>(P.K);
+  // tokens [a_rows, K] bf16 as (element in k-block, row, 64-element k-block)
+  for (int small = 0; small < 2; ++small) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(P.a_rows), K / 64};
+    const uint64_t str[2] = {K * 2, 128};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(small ? SMALL_N : TM), TOK_KBLK};
+    MOE_TRY(encode_tmap_nd(small ? &prm.tma_asf[slot] : &prm.tma_a[slot], P.A, true, 3, dims, str, box, true));
+  }
+  if (swiglu) {
+    // codes [groups][gate N | up N][K/2] as (byte, row, gate/up + 2*group)
+    const uint64_t N = static_cast<uint64_t>(P.N), g2 = 2 * static_cast<uint64_t>(P.groups);
+    const uint64_t dims[3] = {K / 2, N, g2};
+    const uint64_t str[2] = {K / 2, N * (K / 2)};
+    const uint32_t box[3] = {KS / 2, WM / 2, 2};
+    MOE_TRY(encode_tmap_nd(&prm.tma_w[slot], P.W, false, 3, dims, str, box, true));
+    const uint64_t sdims[3] = {K / 16, N, g2};
+    const uint64_t sstr[2] = {K / 16, N * (K / 16)};
+    const uint32_t sbox[3] = {KS / 16, WM / 2, 2};
+    MOE_TRY(encode_tmap_nd(&prm.tma_wsf[slot], P.W_sf, false, 3, sdims, sstr, sbox, false));
+  } else {
+    MOE_TRY(encode_tmap_2d(&prm.tma_w[slot], P.W, 1, K / 2, static_cast<uint64_t>(q.w_rows_total), KS / 2, WM, true));
+    MOE_TRY(encode_tmap_2d(&prm.tma_wsf[slot], P.W_sf, 1, K / 16, static_cast<uint64_t>(q.w_rows_total), KS / 16, WM,
+                           false));
+  }
+  return MOE_OK;
+}
+
+}  // namespace gw4
+
+// bf16 activations x NVFP4 weights with K % 256 == 0 and 16-byte aligned
+// weight scales (checked by the caller, grouped_gemm_launch).
+int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
+                              const GemmProblem* sh, int shared_rows, cudaStream_t s) {
+  gg::Params prm;
+  memset(&prm, 0, sizeof(prm));
+  MOE_TRY(gw4::fill(prm, 0, epi, routed));
+  prm.offsets = offsets;
+  prm.G = G;
+  prm.shared_rows = -1;
+  if (sh != nullptr && shared_rows > 0) {
+    MOE_TRY(gw4::fill(prm, 1, epi, *sh));
+    prm.shared_rows = shared_rows;
+  }
+  prm.err = device_error_word();
+  if (!prm.err) return MOE_ERR_CUDA;
+  prm.timeout_ns = wait_timeout_ns();
+  if (epi == MOE_EPI_STORE_BF16) return gw4::launch<MOE_EPI_STORE_BF16>(prm, s);
+  if (epi == kEpiSwigluF16) return gw4::launch<kEpiSwigluF16>(prm, s);
+  return gw4::launch<MOE_EPI_SWIGLU_BF16>(prm, s);
+}
+
+}  // namespace moe

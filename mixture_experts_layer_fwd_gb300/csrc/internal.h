@@ -6,9 +6,10 @@
 namespace moe {
 
 size_t permute_ws_bytes(int T, int k, int E);
+// to_f16: the rows are bf16 and are written to xp_rows as fp16 (saturating).
 int permute_launch(const int32_t* idx, int T, int k, int E, const void* x_rows, int row_bytes, const uint8_t* x_sf,
                    int sf_row_bytes, int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
-                   void* xp_rows, uint8_t* xp_sf, void* ws, size_t ws_bytes, cudaStream_t s);
+                   void* xp_rows, uint8_t* xp_sf, void* ws, size_t ws_bytes, cudaStream_t s, bool to_f16 = false);
 
 size_t quant_ws_bytes(int groups);
 int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float* g_in, uint8_t* codes, uint8_t* sf,
@@ -32,7 +33,12 @@ struct GemmProblem {
   uint8_t* C_sf;       // [a_rows, N/16] (NVFP4 C)
   const float* c_g;    // device scalar (NVFP4 C)
   int N, K;
+  bool a_f16 = false;  // bf16-activation problems: A already holds fp16 (layer-internal)
 };
+
+// Layer-internal epilogue of the NVFP4-weight / bf16-activation path: SwiGLU
+// with h stored as fp16 for the down projection's fp16 MMA.
+constexpr int kEpiSwigluF16 = 16;
 
 int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed, const int32_t* offsets, int G,
                         const GemmProblem* sh, int shared_rows, cudaStream_t s);
@@ -46,6 +52,10 @@ int grouped_gemm_launch_pair(int epi, const GemmProblem& routed, const int32_t* 
 // scale arrays are 16-byte aligned, else to gemm_fp4.cu's kernel.
 int grouped_gemm_launch_nvf4(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                              const GemmProblem* sh, int shared_rows, cudaStream_t s);
+// bf16 activations x NVFP4 weights, K % 256 == 0: weights expanded into
+// tensor memory, fp16 MMA (gemm_w4a16.cu).
+int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
+                              const GemmProblem* sh, int shared_rows, cudaStream_t s);
 int grouped_gemm_launch_nvf4_wide(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                                   const GemmProblem* sh, int shared_rows, cudaStream_t s);
 

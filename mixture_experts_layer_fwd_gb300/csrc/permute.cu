@@ -121,8 +121,21 @@ __global__ void __launch_bounds__(32) permute_assign_kernel(const int32_t* __res
   }
 }
 
+DEVINL uint32_t bf16x2_to_f16x2_satfinite(uint32_t v) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(v & 0xFFFF0000u)),
+      "f"(__uint_as_float(v << 16)));
+  return r;
+}
+DEVINL uint4 cvt_row_vec(uint4 v, bool to_f16) {
+  if (!to_f16) return v;
+  return make_uint4(bf16x2_to_f16x2_satfinite(v.x), bf16x2_to_f16x2_satfinite(v.y), bf16x2_to_f16x2_satfinite(v.z),
+                    bf16x2_to_f16x2_satfinite(v.w));
+}
+
 // One warp per permuted row; copies row_bytes (multiple of 16) and sf bytes
-// (multiple of 4).
+// (multiple of 4).  to_f16: the row holds bf16 values, written as fp16.
+template <bool TO_F16>
 __global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __restrict__ src_tok, int S,
                                                              const uint8_t* __restrict__ x, int row_bytes,
                                                              const uint8_t* __restrict__ x_sf, int sf_bytes,
@@ -137,12 +150,12 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __re
   int i = lane;
   for (; i + 96 < nvec; i += 128) {
     const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
-    dst[i] = a;
-    dst[i + 32] = b;
-    dst[i + 64] = c;
-    dst[i + 96] = d;
+    dst[i] = cvt_row_vec(a, TO_F16);
+    dst[i + 32] = cvt_row_vec(b, TO_F16);
+    dst[i + 64] = cvt_row_vec(c, TO_F16);
+    dst[i + 96] = cvt_row_vec(d, TO_F16);
   }
-  for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
+  for (; i < nvec; i += 32) dst[i] = cvt_row_vec(__ldg(src + i), TO_F16);
   if (x_sf != nullptr) {
     const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(x_sf + static_cast<size_t>(t) * sf_bytes);
     uint32_t* sdst = reinterpret_cast<uint32_t*>(xp_sf + static_cast<size_t>(r) * sf_bytes);
@@ -158,7 +171,7 @@ size_t permute_ws_bytes(int T, int k, int E) {
 
 int permute_launch(const int32_t* idx, int T, int k, int E, const void* x_rows, int row_bytes, const uint8_t* x_sf,
                    int sf_row_bytes, int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
-                   void* xp_rows, uint8_t* xp_sf, void* ws, size_t ws_bytes, cudaStream_t s) {
+                   void* xp_rows, uint8_t* xp_sf, void* ws, size_t ws_bytes, cudaStream_t s, bool to_f16) {
   const int S = T * k;
   const int C = (S + kPermChunk - 1) / kPermChunk;
   Carve carve(ws, ws_bytes);
@@ -171,8 +184,12 @@ int permute_launch(const int32_t* idx, int T, int k, int E, const void* x_rows, 
   if (C > 0) permute_assign_kernel<<<C, 32, shbytes, s>>>(idx, S, k, E, base, row_of, src_tok);
   if (xp_rows != nullptr && S > 0) {
     const int blocks = (S + 7) / 8;
-    permute_gather_kernel<<<blocks, 256, 0, s>>>(src_tok, S, static_cast<const uint8_t*>(x_rows), row_bytes, x_sf,
-                                                 sf_row_bytes, static_cast<uint8_t*>(xp_rows), xp_sf);
+    if (to_f16)
+      permute_gather_kernel<true><<<blocks, 256, 0, s>>>(src_tok, S, static_cast<const uint8_t*>(x_rows), row_bytes,
+                                                         x_sf, sf_row_bytes, static_cast<uint8_t*>(xp_rows), xp_sf);
+    else
+      permute_gather_kernel<false><<<blocks, 256, 0, s>>>(src_tok, S, static_cast<const uint8_t*>(x_rows), row_bytes,
+                                                          x_sf, sf_row_bytes, static_cast<uint8_t*>(xp_rows), xp_sf);
   }
   return check_launch();
 }

@@ -271,23 +271,28 @@ def test_grouped_gemm_bf16_token_blocks(epi):
     assert row_err.max() < 2e-2, int(row_err.argmax())
 
 
-def test_grouped_gemm_nvfp4_weights():
-    """bf16 A x NVFP4 W (codes + E4M3 scales + per-group fp32 scale)."""
+@pytest.mark.parametrize("epi,N,K", [(1, 256, 512), (0, 384, 768), (1, 192, 320), (0, 128, 576)])
+def test_grouped_gemm_nvfp4_weights(epi, N, K):
+    """bf16 A x NVFP4 W (codes + E4M3 scales + per-group fp32 scale): K a
+    multiple of 256 (weights expanded into tensor memory, fp16 MMA) and not
+    (converter kernel, bf16 MMA); ragged groups past 64 tokens and empty ones."""
     m = api()
-    counts = [3, 200, 0, 64, 129]
+    counts = [3, 200, 0, 64, 129, 17]
     offs = _ragged_offsets(counts)
-    M, G, N, K = int(offs[-1]), len(counts), 256, 512
-    g = torch.Generator().manual_seed(21)
+    M, G = int(offs[-1]), len(counts)
+    Wn = 2 * N if epi == 1 else N
+    g = torch.Generator().manual_seed(21 + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
-    Wb = (torch.randn(G, 2 * N, K, generator=g) * 0.02).to(torch.bfloat16)
+    Wb = (torch.randn(G, Wn, K, generator=g) * 0.02).to(torch.bfloat16)
     Wq = [nvfp4.quantize(to_np_f32(Wb[i])) for i in range(G)]  # oracle's encoding of the weights
     codes = torch.from_numpy(np.stack([q for q, _, _ in Wq]))
     sf = torch.from_numpy(np.stack([s for _, s, _ in Wq]))
     gw = torch.tensor([gg for _, _, gg in Wq], dtype=torch.float32)
-    C = m.moe_grouped_gemm(0, 1, 1, offs.to(DEV), N, K, A.to(DEV), codes.to(DEV), W_sf=sf.to(DEV), W_g=gw.to(DEV))
+    C = m.moe_grouped_gemm(0, 1, epi, offs.to(DEV), N, K, A.to(DEV), codes.to(DEV), W_sf=sf.to(DEV),
+                           W_g=gw.to(DEV))
     _sync()
     Wd = np.stack([nvfp4.dequantize(q, s, gg) for q, s, gg in Wq])
-    ref = _gemm_ref(A.double().numpy(), Wd, offs.numpy(), True, N)
+    ref = _gemm_ref(A.double().numpy(), Wd, offs.numpy(), epi == 1, N)
     err = oracle.rel_frobenius(C.float().cpu().numpy(), ref)
     assert err < 5e-3, err
 
