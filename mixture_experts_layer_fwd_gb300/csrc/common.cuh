@@ -390,15 +390,6 @@ DEVINL void tmem_st_32x32b_x64(uint32_t taddr, const uint32_t (&r)[64]) {
       "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
       : "memory");
 }
-// Two E2M1 codes (low nibble = first element) -> two fp16 (exact).
-DEVINL uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tmov.b16 {t, _}, h;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(byte));
-  return r;
-}
 // Two E4M3 bytes (low byte = first) -> two fp16 (exact).
 DEVINL uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   uint32_t r;

@@ -18,9 +18,10 @@
 // can read its A operand from tensor memory instead (tcgen05.mma [a-tmem]).
 //
 // Tiles: weights on the MMA's M side (128 weight rows), tokens on N (a group
-// of r routed rows is cut into ceil(r/64) equal token blocks rounded up to
-// 16; N <= 64), so a weight tile is expanded once per 64 tokens and a decode
-// step (a few tokens per expert) streams each weight once.
+// of r routed rows is cut into ceil(r/TM) equal token blocks rounded up to
+// 16; TM = 64, or 16 when the launch averages at most 4 routed rows per
+// expert), so a weight tile is expanded once per TM tokens and a decode step
+// (a few tokens per expert) streams each weight once.
 //
 // Roles (one CTA per SM):
 //   warp 0       TMA producer, per 256-element k stage: the tile's packed
@@ -54,21 +55,16 @@ using gg::Params;
 using gg::Prob;
 
 constexpr int WM = 128;                   // weight rows per tile (M of the MMA)
-constexpr int TM = 64;                    // most tokens per tile (N of the MMA)
 constexpr int SMALL_N = 16;               // tiles of <= 16 tokens stage 16 token rows
 constexpr int KS = 256;                   // elements per stage
 constexpr int CODE_TILE = WM * KS / 2;    // 16 KB of packed E2M1
 constexpr int SF_TILE = WM * KS / 16;     // 2 KB: 16 scale bytes per row
 constexpr int TOK_KBLK = KS / 64;         // 64-element k-blocks of tokens per stage
-constexpr int TOK_TILE = TM * KS * 2;     // 32 KB: up to 64 token rows
 constexpr int OFF_SF = CODE_TILE;
 constexpr int OFF_TOK = CODE_TILE + SF_TILE;
-constexpr int STAGE_BYTES = OFF_TOK + TOK_TILE;
-constexpr int STAGES = 4;
-constexpr int ASLOTS = 3;                 // expanded-weight slots in tensor memory
-constexpr int ACC_COLS = TM;              // accumulator columns per buffer
 constexpr int A_COLS = KS / 2;            // fp16 pairs per row per stage
-constexpr int A_COL0 = 2 * ACC_COLS;
+constexpr int A_COL0 = 128;               // expanded-weight slots start here
+constexpr int ASLOTS = 3;                 // expanded-weight slots in tensor memory
 constexpr int TMEM_COLS = 512;
 constexpr int CONV_WARPS = 8;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
@@ -77,16 +73,32 @@ constexpr int THREADS = NUM_WARPS * 32;
 constexpr int XCH_FLOATS = 32 * 32;
 constexpr int XCH_BYTES = 2 * 2 * XCH_FLOATS * 4;
 constexpr int EXTRA = (256 + 4 * 2 * (MAX_G + 4) + 15) & ~15;
-constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA + XCH_BYTES + 64;
-static_assert(OFF_TOK % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(OFF_TOK % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(A_COL0 + ASLOTS * A_COLS <= TMEM_COLS, "tensor memory budget");
-static_assert(SMEM <= 232448, "shared memory budget");
+
+// Two shapes of the same pipeline: TM = 64 tokens per tile (prefill-like
+// launches), and TM = 16 for launches with a few tokens per expert, whose
+// smaller stages (26 KB instead of 50 KB) let 7 stages be in flight instead
+// of 4 while each stage waits on HBM.
+template <int TMT>
+struct Cfg {
+  static constexpr int TM = TMT;                         // most tokens per tile (N of the MMA)
+  static constexpr int TOK_TILE = TMT * KS * 2;
+  static constexpr int STAGE_BYTES = OFF_TOK + TOK_TILE;
+  static constexpr int STAGES = TMT == SMALL_N ? 7 : 4;
+  static constexpr int ACC_COLS = TMT;                   // accumulator columns per buffer
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA + XCH_BYTES + 64;
+  static_assert(STAGE_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(2 * ACC_COLS <= A_COL0, "tensor memory budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
 
 struct Tile {
   int pb, g, row0, cnt, n, blk;
 };
 
 // As the bf16 pair kernel's schedule, with token blocks of at most TM rows.
+template <int TM>
 DEVINL Tile decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
   int lo = 0, hi = GT;
   while (hi - lo > 1) {
@@ -150,9 +162,13 @@ DEVINL void store_pairs(const Prob& P, const float (&h)[NV], int col, int row_fi
   }
 }
 
-template <int EPI>
+template <int EPI, int TMT>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __grid_constant__ Params p) {
-  constexpr int S = STAGES;
+  using C = Cfg<TMT>;
+  constexpr int TM = C::TM;
+  constexpr int S = C::STAGES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int ACC_COLS = C::ACC_COLS;
   constexpr bool SWIGLU = EPI != MOE_EPI_STORE_BF16;
   constexpr bool OUT_F16 = EPI == kEpiSwigluF16;
   extern __shared__ uint8_t smem_raw[];
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
       for (int s = 0; s < S; ++s) issued[s] = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
         const Prob& P = p.prob[ti.pb];
         const bool small = ti.n <= SMALL_N;
         const void* tt = small ? &p.tma_asf[ti.pb] : &p.tma_a[ti.pb];
@@ -271,7 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
     uint32_t phase = 0, sphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
       const int nk = p.prob[ti.pb].K / KS;
       const int kstride = (ti.n <= SMALL_N ? SMALL_N : TM) * 128;
       // 16-byte chunks of the token rows the MMA reads, when given in bf16
@@ -310,9 +326,14 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
             const uint32_t sc = wi < 2 ? s_lo : s_hi;
+            uint32_t o[4];
+            asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+                "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+                "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+                : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+                : "r"(words[wi]));
 #pragma unroll
-            for (int bi = 0; bi < 4; ++bi)
-              r[c4 * 16 + wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xFFu), sc);
+            for (int bi = 0; bi < 4; ++bi) r[c4 * 16 + wi * 4 + bi] = hmul2_u32(o[bi], sc);
           }
         }
         tmem_st_32x32b_x64(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -341,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
       bool ok = true;
       int it = 0;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
         const int nk = p.prob[ti.pb].K / KS;
         const uint32_t idesc = idesc_f16_f32(WM, ti.n);
         const uint32_t kstride = static_cast<uint32_t>((ti.n <= SMALL_N ? SMALL_N : TM) * 128);
@@ -393,7 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
     float* x_to_gate = x_to_up + XCH_FLOATS;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
       const Prob& P = p.prob[ti.pb];
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -473,25 +494,30 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
   }
 }
 
-template <int EPI>
+template <int EPI, int TMT>
 static int launch(const Params& prm, cudaStream_t s) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(grouped_gemm_w4a16_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_w4a16_kernel<EPI, TMT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<TMT>::SMEM);
     if (e != cudaSuccess) {
       set_cuda_error(e);
       return MOE_ERR_CUDA;
     }
     attr_done[dev] = true;
   }
-  grouped_gemm_w4a16_kernel<EPI><<<num_sms(), THREADS, SMEM, s>>>(prm);
+  grouped_gemm_w4a16_kernel<EPI, TMT><<<num_sms(), THREADS, Cfg<TMT>::SMEM, s>>>(prm);
   return check_launch();
 }
 
-static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
+template <int EPI>
+static int launch_shape(const Params& prm, bool small, cudaStream_t s) {
+  return small ? launch<EPI, SMALL_N>(prm, s) : launch<EPI, 64>(prm, s);
+}
+
+static int fill(Params& prm, int slot, int epi, const GemmProblem& P, int tm) {
   Prob& q = prm.prob[slot];
   const bool swiglu = epi != MOE_EPI_STORE_BF16;
   const int tn = swiglu ? WM / 2 : WM;  // output columns per weight tile
@@ -514,7 +540,7 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
   for (int small = 0; small < 2; ++small) {
     const uint64_t dims[3] = {64, static_cast<uint64_t>(P.a_rows), K / 64};
     const uint64_t str[2] = {K * 2, 128};
-    const uint32_t box[3] = {64, static_cast<uint32_t>(small ? SMALL_N : TM), TOK_KBLK};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(small ? SMALL_N : tm), TOK_KBLK};
     MOE_TRY(encode_tmap_nd(small ? &prm.tma_asf[slot] : &prm.tma_a[slot], P.A, true, 3, dims, str, box, true));
   }
   if (swiglu) {
@@ -544,20 +570,25 @@ int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t*
                               const GemmProblem* sh, int shared_rows, cudaStream_t s) {
   gg::Params prm;
   memset(&prm, 0, sizeof(prm));
-  MOE_TRY(gw4::fill(prm, 0, epi, routed));
+  // a few routed rows per expert (decode): 16-token tiles and a deeper
+  // pipeline; from ~10 rows per expert on, splitting the busier groups into
+  // 16-token tiles re-expands their weights more often than it gains
+  const bool small = static_cast<long long>(routed.a_rows) <= 4ll * G;
+  const int tm = small ? gw4::SMALL_N : 64;
+  MOE_TRY(gw4::fill(prm, 0, epi, routed, tm));
   prm.offsets = offsets;
   prm.G = G;
   prm.shared_rows = -1;
   if (sh != nullptr && shared_rows > 0) {
-    MOE_TRY(gw4::fill(prm, 1, epi, *sh));
+    MOE_TRY(gw4::fill(prm, 1, epi, *sh, tm));
     prm.shared_rows = shared_rows;
   }
   prm.err = device_error_word();
   if (!prm.err) return MOE_ERR_CUDA;
   prm.timeout_ns = wait_timeout_ns();
-  if (epi == MOE_EPI_STORE_BF16) return gw4::launch<MOE_EPI_STORE_BF16>(prm, s);
-  if (epi == kEpiSwigluF16) return gw4::launch<kEpiSwigluF16>(prm, s);
-  return gw4::launch<MOE_EPI_SWIGLU_BF16>(prm, s);
+  if (epi == MOE_EPI_STORE_BF16) return gw4::launch_shape<MOE_EPI_STORE_BF16>(prm, small, s);
+  if (epi == kEpiSwigluF16) return gw4::launch_shape<kEpiSwigluF16>(prm, small, s);
+  return gw4::launch_shape<MOE_EPI_SWIGLU_BF16>(prm, small, s);
 }
 
 }  // namespace moe

@@ -271,13 +271,15 @@ def test_grouped_gemm_bf16_token_blocks(epi):
     assert row_err.max() < 2e-2, int(row_err.argmax())
 
 
-@pytest.mark.parametrize("epi,N,K", [(1, 256, 512), (0, 384, 768), (1, 192, 320), (0, 128, 576)])
-def test_grouped_gemm_nvfp4_weights(epi, N, K):
+@pytest.mark.parametrize("epi,N,K,few", [(1, 256, 512, False), (0, 384, 768, False), (1, 192, 320, False),
+                                         (0, 128, 576, False), (1, 256, 1024, True), (0, 512, 256, True)])
+def test_grouped_gemm_nvfp4_weights(epi, N, K, few):
     """bf16 A x NVFP4 W (codes + E4M3 scales + per-group fp32 scale): K a
-    multiple of 256 (weights expanded into tensor memory, fp16 MMA) and not
-    (converter kernel, bf16 MMA); ragged groups past 64 tokens and empty ones."""
+    multiple of 256 (weights expanded into tensor memory, fp16 MMA; 64-token
+    tiles, or 16-token tiles when the groups average <= 4 rows) and not
+    (converter kernel, bf16 MMA); ragged groups past a tile and empty ones."""
     m = api()
-    counts = [3, 200, 0, 64, 129, 17]
+    counts = [1, 2, 0, 20, 3, 2, 1, 0, 5, 1] if few else [3, 200, 0, 64, 129, 17]
     offs = _ragged_offsets(counts)
     M, G = int(offs[-1]), len(counts)
     Wn = 2 * N if epi == 1 else N
