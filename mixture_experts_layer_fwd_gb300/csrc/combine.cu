@@ -4,20 +4,27 @@
 // Blackwell", section "MoE Dispatch - Combine": weighted accumulation after
 // the MoE GEMM).
 //
-// One warp per token; each lane owns 8-element (16-byte) column chunks and
-// accumulates, in fp32 and in the fixed order j = 0..k-1 then the shared
-// expert, w[t,j] * Y[row_of[t,j]] before one round to bf16.  HBM-bound:
-// reads k + 1 rows, writes one.
+// One warp per (token, 256-column slice): lane l owns the slice's 8-element
+// (16-byte) chunk l.  In fp32 and in the fixed order j = 0..k-1 then the
+// shared expert, it accumulates w[t,j] * Y[row_of[t,j]] before one round to
+// bf16.  HBM-bound: reads k + 1 rows, writes one.  The slice split keeps
+// enough warps in flight at decode sizes (a few hundred tokens), and the k
+// rows' loads are issued in batches of 8 before their FMAs.
 #include "internal.h"
 
 namespace moe {
 
+constexpr int kCombineBatch = 8;
+
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ w, const uint16_t* __restrict__ Ys,
-                                                      int T, int k, int H, uint16_t* __restrict__ out) {
-  const int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+                                                      int T, int k, int H, int slices, uint16_t* __restrict__ out) {
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  const int t = static_cast<int>(gw / slices);
   if (t >= T) return;
+  const int c = static_cast<int>(gw - static_cast<long long>(t) * slices) * 32 + lane;  // 16-byte chunk
+  const bool valid = c < (H >> 3);
   // lane j < k holds the j-th row / weight; broadcast by shuffles
   int my_row = 0;
   float my_w = 0.0f;
@@ -25,45 +32,57 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     my_row = __ldg(row_of + static_cast<size_t>(t) * k + lane);
     my_w = __ldg(w + static_cast<size_t>(t) * k + lane);
   }
-  const int nvec = H >> 3;
-  for (int c = lane; c < nvec; c += 32) {
-    float acc[8];
+  float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+    uint4 v[kCombineBatch];
+    float wj[kCombineBatch];
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const int j = min(j0 + u, k - 1);
       const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
-      const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(Y + static_cast<size_t>(r) * H) + c);
-      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+      wj[u] = __shfl_sync(0xFFFFFFFFu, my_w, j);
+      v[u] = (valid && j0 + u < k) ? __ldg(reinterpret_cast<const uint4*>(Y + static_cast<size_t>(r) * H) + c)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      if (j0 + u >= k) break;
+      const uint32_t q[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(wj, __uint_as_float(q[i] << 16), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        acc[2 * i] = fmaf(wj[u], __uint_as_float(q[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj[u], __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
       }
     }
-    if (Ys != nullptr) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(Ys + static_cast<size_t>(t) * H) + c);
-      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] += __uint_as_float(q[i] << 16);
-        acc[2 * i + 1] += __uint_as_float(q[i] & 0xFFFF0000u);
-      }
-    }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c] = o;
   }
+  if (!valid) return;
+  if (Ys != nullptr) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(Ys + static_cast<size_t>(t) * H) + c);
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += __uint_as_float(q[i] << 16);
+      acc[2 * i + 1] += __uint_as_float(q[i] & 0xFFFF0000u);
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c] = o;
 }
 
 int combine_launch(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, int T, int k, int H,
                    uint16_t* out, cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  const int blocks = (T + 7) / 8;
-  combine_kernel<<<blocks, 256, 0, s>>>(Y, row_of, w, Ys, T, k, H, out);
+  const int slices = (H / 8 + 31) / 32;
+  const long long warps = static_cast<long long>(T) * slices;
+  const long long blocks = (warps + 7) / 8;
+  if (blocks > 0x7FFFFFFFLL) return MOE_ERR_UNSUPPORTED;
+  combine_kernel<<<static_cast<unsigned int>(blocks), 256, 0, s>>>(Y, row_of, w, Ys, T, k, H, slices, out);
   return check_launch();
 }
 

@@ -66,7 +66,13 @@ constexpr int A_COLS = KS / 2;            // fp16 pairs per row per stage
 constexpr int A_COL0 = 128;               // expanded-weight slots start here
 constexpr int ASLOTS = 3;                 // expanded-weight slots in tensor memory
 constexpr int TMEM_COLS = 512;
+// 4 lane quadrants x KPARTS parts of the stage's K (16 warps measured slower:
+// the register cap of a 704-thread block spills the epilogue)
 constexpr int CONV_WARPS = 8;
+constexpr int KPARTS = CONV_WARPS / 4;
+constexpr int PART_COLS = A_COLS / KPARTS;       // fp16 pairs a converter thread writes per stage
+constexpr int PART_CHUNKS = 8 / KPARTS;          // 16-byte code chunks (32 values) per part
+constexpr int PART_SF_WORDS = 4 / KPARTS;        // 32-bit words of scale bytes per part
 constexpr int CONV_THREADS = CONV_WARPS * 32;
 constexpr int NUM_WARPS = 6 + CONV_WARPS;
 constexpr int THREADS = NUM_WARPS * 32;
@@ -128,6 +134,9 @@ DEVINL uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
   asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+
+DEVINL void tmem_st_part(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st_32x32b_x64(taddr, r); }
+DEVINL void tmem_st_part(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st_32x32b_x32(taddr, r); }
 
 DEVINL uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -281,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
     const int cw = warp - 6;
     const int ctid = cw * 32 + lane;
     const int q = warp & 3;          // TMEM lane quadrant
-    const int kh = cw >> 2;          // half of the stage's K this warp expands
+    const int kh = cw >> 2;          // part of the stage's K this warp expands
     const int row = q * 32 + lane;   // weight row of the tile = TMEM lane
     int stage = 0, slot = 0;
     uint32_t phase = 0, sphase = 0;
@@ -311,15 +320,18 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
           v.w = bf16x2_to_f16x2_sat(v.w);
           *ptr = v;
         }
-        // weights: this thread's row, elements [kh*128, +128) of the stage
+        // weights: this thread's row, elements [kh*256/KPARTS, +256/KPARTS) of the stage
         const uint8_t* crow = sb + row * 128;
-        const uint2 sw = *reinterpret_cast<const uint2*>(sb + OFF_SF + row * 16 + kh * 8);
-        uint32_t r[64];
+        uint32_t sw[PART_SF_WORDS];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int j = 4 * kh + c4;  // 16-byte chunk of the row (32 elements, two scale blocks)
+        for (int i = 0; i < PART_SF_WORDS; ++i)
+          sw[i] = *reinterpret_cast<const uint32_t*>(sb + OFF_SF + row * 16 + kh * 4 * PART_SF_WORDS + 4 * i);
+        uint32_t r[PART_COLS];
+#pragma unroll
+        for (int c4 = 0; c4 < PART_CHUNKS; ++c4) {
+          const int j = PART_CHUNKS * kh + c4;  // 16-byte chunk of the row (32 elements, two scale blocks)
           const uint4 cv = *reinterpret_cast<const uint4*>(crow + ((j ^ (row & 7)) << 4));
-          const uint32_t sbytes = ((c4 < 2 ? sw.x : sw.y) >> (16 * (c4 & 1))) & 0xFFFFu;
+          const uint32_t sbytes = (sw[c4 >> 1] >> (16 * (c4 & 1))) & 0xFFFFu;
           const uint32_t s2 = e4m3x2_to_f16x2(sbytes);
           const uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
           const uint32_t words[4] = {cv.x, cv.y, cv.z, cv.w};
@@ -336,9 +348,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
             for (int bi = 0; bi < 4; ++bi) r[c4 * 16 + wi * 4 + bi] = hmul2_u32(o[bi], sc);
           }
         }
-        tmem_st_32x32b_x64(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(A_COL0 + slot * A_COLS + kh * 64),
-                           r);
+        const uint32_t a_dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(A_COL0 + slot * A_COLS + kh * PART_COLS);
+        tmem_st_part(a_dst, r);
         tmem_st_wait();
         fence_proxy_async_smem();  // the converted tokens are read by the MMA (async proxy)
         tc_fence_before();

@@ -52,9 +52,16 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int e0 = 0; e0 < E; e0 += blockDim.x) {
     const int e = e0 + threadIdx.x;
+    // the chunk histograms are read 8 at a time so that the loads overlap
     int tot = 0;
     if (e < E)
-      for (int c = 0; c < C; ++c) tot += hist[static_cast<size_t>(c) * E + e];
+      for (int c0 = 0; c0 < C; c0 += 8) {
+        int h8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) h8[u] = (c0 + u < C) ? __ldg(hist + static_cast<size_t>(c0 + u) * E + e) : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) tot += h8[u];
+      }
     // block-wide inclusive scan of tot
     int v = tot;
 #pragma unroll
@@ -79,9 +86,15 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
       counts[e] = tot;
       offsets[e] = excl;
       int run = excl;
-      for (int c = 0; c < C; ++c) {
-        base[static_cast<size_t>(c) * E + e] = run;
-        run += hist[static_cast<size_t>(c) * E + e];
+      for (int c0 = 0; c0 < C; c0 += 8) {
+        int h8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) h8[u] = (c0 + u < C) ? __ldg(hist + static_cast<size_t>(c0 + u) * E + e) : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (c0 + u < C) base[static_cast<size_t>(c0 + u) * E + e] = run;
+          run += h8[u];
+        }
       }
     }
     __syncthreads();
@@ -103,12 +116,22 @@ __global__ void __launch_bounds__(32) permute_assign_kernel(const int32_t* __res
   __syncwarp();
   const int lo = c * kPermChunk;
   const int hi = min(S, lo + kPermChunk);
-  for (int s0 = lo; s0 < hi; s0 += 32) {
-    const int s = s0 + lane;
+  // the chunk's routing ids, loaded up front (lane l holds slots lo + 32j + l)
+  constexpr int J = kPermChunk / 32;
+  int ev[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int s = lo + 32 * j + lane;
+    ev[j] = s < hi ? __ldg(idx + s) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int s = lo + 32 * j + lane;
+    if (lo + 32 * j >= hi) break;
     const bool act = s < hi;
     const unsigned mask = __ballot_sync(0xFFFFFFFFu, act);
     if (act) {
-      const int e = __ldg(idx + s);
+      const int e = ev[j];
       const unsigned peers = __match_any_sync(mask, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       const int pos = ctr[e] + rank;
