@@ -449,6 +449,67 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """--sweep: the size and load-imbalance sweep on DeepSeek-V3 shapes
+    (T = 1..65536 in powers of 2, router-bias Zipf exponent 0 / 1.1 / 2.0,
+    bf16 weights with bf16 activations and NVFP4 weights with NVFP4
+    activations).  One JSON line per point.  The weights of a format are built
+    once; each point runs on the first T tokens of one seeded 65536-token batch
+    per Zipf exponent (rows are token-independent, so the prefix is a T-token
+    batch of the same distribution).  Not the benchmark line."""
+    from mixture_experts_layer_fwd_gb300 import MoELayer, api, moe_sync_status
+    from mixture_experts_layer_fwd_gb300 import build as _build
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    _build.build()
+    _, src = peaks()
+    Ts = [int(t) for t in args.sweep_ts.split(",")] if args.sweep_ts else list(synth.SWEEP_TS)
+    fmts = [args.w_fmt] if args.w_fmt else ["bf16", "nvfp4"]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    Tmax = max(Ts)
+    for fmt in fmts:
+        cfg0 = synth.sweep_config(fmt, 1.1)
+        w = synth.make_weights(cfg0, seed=0, device=str(dev))
+        layer = MoELayer.from_config(cfg0, w)
+        del w
+        torch.cuda.empty_cache()
+        ws = layer.workspace(Tmax)
+        out_full = torch.empty(Tmax, cfg0.H, dtype=torch.bfloat16, device=dev)
+        for z in synth.SWEEP_ZIPF:
+            cfg = synth.sweep_config(fmt, z)
+            acts = synth.make_activations(cfg, Tmax, seed=0)
+            x_full, lg_full = acts.x.to(dev), acts.logits.to(dev)
+            for T in Ts:
+                x, lg, out = x_full[:T].contiguous(), lg_full[:T].contiguous(), out_full[:T]
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+                for ev in evs:
+                    ev.record()
+                steps = args.sweep_steps
+                res = []
+                for i in range(args.warmup + steps):
+                    flush.zero_()
+                    api.moe_forward_profiled(layer.c, x, lg, out, ws, evs)
+                    torch.cuda.synchronize()
+                    if i >= args.warmup:
+                        res.append((evs[0].elapsed_time(evs[6]), evs[3].elapsed_time(evs[5])))
+                if moe_sync_status() != 0:
+                    raise RuntimeError(f"device status not clean at {fmt} z={z} T={T}")
+                idx, _ = api.moe_route(lg, cfg.k)
+                active = int((torch.bincount(idx.reshape(-1).long(), minlength=cfg.E) > 0).sum())
+                ms = float(np.median([r[0] for r in res]))
+                gms = float(np.median([r[1] for r in res]))
+                roof = roofline(cfg, T, gms, active, None, src)
+                print(json.dumps({"sweep": "deepseek-v3 shapes", "w_fmt": fmt, "act_fmt": cfg.act_fmt, "zipf": z,
+                                  "T": T, "active_experts": active, "ms_per_step": round(ms, 4),
+                                  "tokens_per_s": round(T / (ms / 1e3), 1), "gemm_ms": round(gms, 4),
+                                  "roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "frac")}}),
+                      flush=True)
+            del x_full, lg_full
+        del layer, ws, out_full
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -464,6 +525,10 @@ def main():
     ap.add_argument("--T", type=int, default=None, help="tokens (default: the workload's largest)")
     ap.add_argument("--zipf", type=float, default=None, help="router-bias Zipf exponent override")
     ap.add_argument("--w-fmt", default=None, choices=["bf16", "nvfp4"], help="sweep weight format")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the DeepSeek-V3-shape size / imbalance sweep (one JSON line per point)")
+    ap.add_argument("--sweep-ts", default=None, help="comma-separated T values of the sweep (default 1..65536)")
+    ap.add_argument("--sweep-steps", type=int, default=10, help="timed steps per sweep point")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling variant: this many experts, tokens scaled to keep tokens per expert")
     args = ap.parse_args()
@@ -471,6 +536,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_gpu(args)
 
