@@ -16,7 +16,7 @@
 // Scale factors: one MMA reads its 128 rows' four E4M3 scales from four
 // tensor-memory columns, row r in lane r % 32 (all four lane quadrants) and
 // column r / 32.  The scales arrive by TMA as row slices ([rows, K/16]
-// bytes, 16 bytes = four MMAs per row per 256-element k-block).  Four scale
+// bytes: 32 contiguous bytes = eight MMAs per row per stage).  Four scale
 // warps, one per lane quadrant, gather for their lane l the words of rows
 // l, l+32, l+64, l+96 from the slices and write the stage's 8 MMAs x 4
 // columns with one tcgen05.st per operand (a copy instruction per MMA and
@@ -27,7 +27,7 @@
 //               two 256-element k-blocks as the outer box dimension:
 //               A codes 128 rows x 2 x 128 bytes (128-byte swizzle), B codes
 //               likewise (SwiGLU: 64 gate rows then the 64 up rows of the
-//               same features, per k-block), A scales 2 x 128 rows x 16 bytes,
+//               same features, per k-block), A scales 128 rows x 32 bytes,
 //               B scales likewise
 //   warps 6..9  scale warps (above): sf_full -> shared-memory gather ->
 //               tcgen05.st -> arrive sf_ready (the scale copies are issued
@@ -59,7 +59,7 @@ constexpr int KBLK = 2;                   // k-blocks per stage
 constexpr int KE = KBLK * 256;            // elements per stage
 constexpr int A_TILE = BM * KB_BYTES;     // 16 KB per k-block
 constexpr int B_TILE = BN * KB_BYTES;     // 16 KB per k-block
-constexpr int SF_TILE = 128 * 16;         // 2 KB: 128 rows x 16 scale bytes per k-block
+constexpr int SF_TILE = 128 * 16;         // 2 KB of scale bytes per k-block: 16 per row
 constexpr int OFF_B = KBLK * A_TILE;
 constexpr int OFF_SFA = OFF_B + KBLK * B_TILE;
 constexpr int OFF_SFB = OFF_SFA + KBLK * SF_TILE;
@@ -170,11 +170,11 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
           uint8_t* sb = stages + stage * STAGE_BYTES;
           const int kblk = kb * KBLK;
           mbar_arrive_expect_tx(&sf_full[stage], TX_SF);
-          tma_load_3d(&p.tma_asf[ti.pb], &sf_full[stage], sb + OFF_SFA, 0, a_y, kblk);
+          tma_load_2d(&p.tma_asf[ti.pb], &sf_full[stage], sb + OFF_SFA, kb * 32, a_y);
           if (SWIGLU)
-            tma_load_4d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, 0, f0, 2 * ti.g, kblk);
+            tma_load_3d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, kb * 32, f0, 2 * ti.g);
           else
-            tma_load_3d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, 0, w_y, kblk);
+            tma_load_2d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, kb * 32, w_y);
           mbar_arrive_expect_tx(&full[stage], TX_CODES);
           tma_load_3d(&p.tma_a[ti.pb], &full[stage], sb, 0, a_y, kblk);
           if (SWIGLU)
@@ -273,8 +273,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
           for (int j = 0; j < KBLK; ++j)
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              v[j][c] = *reinterpret_cast<const uint4*>(sb + (op ? OFF_SFB : OFF_SFA) + j * SF_TILE +
-                                                        (lane + 32 * c) * 16);
+              v[j][c] = *reinterpret_cast<const uint4*>(sb + (op ? OFF_SFB : OFF_SFA) + j * 16 +
+                                                        (lane + 32 * c) * 32);
           // column 4m + c of this lane = MMA m's word of row lane + 32c
           uint32_t r[32];
 #pragma unroll
@@ -374,10 +374,7 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
     const uint64_t str[2] = {code_ld, KB_BYTES};
     const uint32_t box[3] = {KB_BYTES, BM, KBLK};
     MOE_TRY(encode_tmap_nd(&prm.tma_a[slot], P.A, false, 3, dims, str, box, true));
-    const uint64_t sdims[3] = {16, static_cast<uint64_t>(P.a_rows), nkb};
-    const uint64_t sstr[2] = {sf_ld, 16};
-    const uint32_t sbox[3] = {16, BM, KBLK};
-    MOE_TRY(encode_tmap_nd(&prm.tma_asf[slot], P.A_sf, false, 3, sdims, sstr, sbox, false));
+    MOE_TRY(encode_tmap_2d(&prm.tma_asf[slot], P.A_sf, 1, sf_ld, static_cast<uint64_t>(P.a_rows), 32, BM, false));
   }
   if (swiglu) {
     // W [groups][gate N | up N][K/2] as (byte, row, gate/up + 2*group, k-block)
@@ -386,20 +383,17 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
     const uint64_t str[3] = {code_ld, N * code_ld, KB_BYTES};
     const uint32_t box[4] = {KB_BYTES, BN / 2, 2, KBLK};
     MOE_TRY(encode_tmap_nd(&prm.tma_w[slot], P.W, false, 4, dims, str, box, true));
-    const uint64_t sdims[4] = {16, N, g2, nkb};
-    const uint64_t sstr[3] = {sf_ld, N * sf_ld, 16};
-    const uint32_t sbox[4] = {16, BN / 2, 2, KBLK};
-    MOE_TRY(encode_tmap_nd(&prm.tma_wsf[slot], P.W_sf, false, 4, sdims, sstr, sbox, false));
+    const uint64_t sdims[3] = {sf_ld, N, g2};
+    const uint64_t sstr[2] = {sf_ld, N * sf_ld};
+    const uint32_t sbox[3] = {32, BN / 2, 2};
+    MOE_TRY(encode_tmap_nd(&prm.tma_wsf[slot], P.W_sf, false, 3, sdims, sstr, sbox, false));
   } else {
     const uint64_t rows = static_cast<uint64_t>(q.w_rows_total);
     const uint64_t dims[3] = {KB_BYTES, rows, nkb};
     const uint64_t str[2] = {code_ld, KB_BYTES};
     const uint32_t box[3] = {KB_BYTES, BN, KBLK};
     MOE_TRY(encode_tmap_nd(&prm.tma_w[slot], P.W, false, 3, dims, str, box, true));
-    const uint64_t sdims[3] = {16, rows, nkb};
-    const uint64_t sstr[2] = {sf_ld, 16};
-    const uint32_t sbox[3] = {16, BN, KBLK};
-    MOE_TRY(encode_tmap_nd(&prm.tma_wsf[slot], P.W_sf, false, 3, sdims, sstr, sbox, false));
+    MOE_TRY(encode_tmap_2d(&prm.tma_wsf[slot], P.W_sf, 1, sf_ld, rows, 32, BN, false));
   }
   return MOE_OK;
 }
