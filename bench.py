@@ -159,6 +159,13 @@ def barrier(world):
         dist.barrier()
 
 
+def dist_teardown(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def max_over_ranks(v: float, world: int, device) -> float:
     if world == 1:
         return v
@@ -166,6 +173,13 @@ def max_over_ranks(v: float, world: int, device) -> float:
     t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(units_per_rank: float, local_s: float, world: int, device) -> tuple[float, float]:
+    """Whole-job throughput of N independent replicas: the units all ranks
+    processed over the slowest rank's time.  Returns (rate, max seconds)."""
+    slowest = max_over_ranks(local_s, world, device)
+    return world * units_per_rank / slowest, slowest
 
 
 def workload(args):
@@ -279,19 +293,24 @@ def cpu_threads() -> int:
 def run_reference(args):
     """--impl reference: the CPU oracle on the bench workload, K timed steps
     of bounded token samples."""
-    world, rank, _ = dist_setup()
-    if rank != 0:
+    # rank 0 alone runs the oracle; the other ranks exit without work and
+    # without joining a process group
+    if int(os.environ.get("RANK", "0")) != 0:
         return
     cfg, T = CFG, T_MAIN
     acts = synth.make_activations(cfg, T, seed=0)
     w = synth.make_weights(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
     w_host = (w.w13.cpu(), w.w2.cpu())
     del w
-    # size the per-step sample so that warmup + steps take about 3 minutes
-    probe = synth.sample_tokens(T, 8, seed=1)
-    _, t8 = oracle_tokens_per_s(cfg, acts, w_host, probe)
+    # size the per-step sample so that warmup + steps take about 3 minutes:
+    # a step costs a fixed part (the routed experts' weights widened to fp64)
+    # plus a part per token, so probe two sample sizes and solve for n
+    _, t8 = oracle_tokens_per_s(cfg, acts, w_host, synth.sample_tokens(T, 8, seed=1))
+    _, t64 = oracle_tokens_per_s(cfg, acts, w_host, synth.sample_tokens(T, 64, seed=2))
+    per_tok = max((t64 - t8) / 56.0, 1e-6)
+    fixed = max(t64 - 64 * per_tok, 0.0)
     budget = 180.0 / max(1, args.steps + args.warmup)
-    n = int(max(1, min(T, 8 * budget / max(t8, 1e-3))))
+    n = int(max(8, min(T, (budget - fixed) / per_tok)))
     times = []
     for i in range(args.warmup + args.steps):
         toks = synth.sample_tokens(T, n, seed=100 + i)
@@ -372,8 +391,8 @@ def run_gpu(args):
 
     step_ms = [evs[0].elapsed_time(evs[6]) for evs in evsets]
     stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(6)] for evs in evsets])
-    total_ms = max_over_ranks(float(sum(step_ms)), world, dev)
-    value = world * T * args.steps / (total_ms / 1e3)
+    value, total_s = job_rate(T * args.steps, float(sum(step_ms)) / 1e3, world, dev)
+    total_ms = total_s * 1e3
 
     idx, _ = api.moe_route(logits, cfg.k)
     active = int((torch.bincount(idx.reshape(-1).long(), minlength=cfg.E) > 0).sum())
@@ -396,7 +415,7 @@ def run_gpu(args):
         t0 = time.perf_counter()
         api.moe_forward_host(layer.c, xh, lh, oh, xd, ld, out, ws)
         e2e_t.append(time.perf_counter() - t0)
-    e2e_s = max_over_ranks(float(np.mean(e2e_t)), world, dev)
+    e2e_value, _ = job_rate(T, float(np.mean(e2e_t)), world, dev)
 
     a4 = cfg.act_fmt == "nvfp4"
     launches = 8 + (2 if a4 else 0)  # route, 4 permute, 2 GEMM, combine (+ amax, quantise)
@@ -413,7 +432,7 @@ def run_gpu(args):
         "roofline": roof,
         "stage_ms": {n: round(float(np.mean(stage_ms[:, i])), 4) for i, n in
                      enumerate(["route", "quant", "permute", "gemm_gate_up", "gemm_down", "combine"])},
-        "e2e": {"value": round(world * T / e2e_s, 1), "unit": UNIT,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
                 "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 2},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
@@ -447,6 +466,7 @@ def run_gpu(args):
                                           f"({dt:.1f} s of fp64 CPU work; rows are token-independent)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    dist_teardown(world)
 
 
 def run_sweep(args):

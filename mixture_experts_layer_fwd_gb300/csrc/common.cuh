@@ -215,6 +215,24 @@ DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" 
 DEVINL void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Named barrier over `threads` threads (whole warps) that also returns the OR
+// of `pred` over them.  The MMA-issuing warps take their go signal this way
+// from a helper warp that does the mbarrier waits: a memory instruction
+// (mbarrier wait or shared load) in the issuing warp queues behind its
+// outstanding tcgen05.mma instructions and stalls the issue for ~150 ns,
+// the named barrier does not.
+DEVINL bool named_bar_red_or(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
 
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
 DEVINL void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
@@ -251,6 +269,27 @@ DEVINL void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same MMA issued by a whole converged warp: every lane computes the
+// (warp-uniform) operands, elect.sync picks the one lane that issues.  Issue
+// from converged code costs far less per MMA than from a single-lane branch
+// (measured on GB300: ~10 ns per M=128 N=16 K=16 MMA alone and ~19 ns next to
+// busy conversion warps, against ~26 and ~52 ns from a lane-0 branch).
+DEVINL void umma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+DEVINL void umma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
 // Arrive on `bar` once every tcgen05 op issued so far by this thread completes.

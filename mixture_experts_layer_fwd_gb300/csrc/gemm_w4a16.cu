@@ -23,19 +23,31 @@
 // expert), so a weight tile is expanded once per TM tokens and a decode step
 // (a few tokens per expert) streams each weight once.
 //
+// Two rings of shared-memory stages, one per 256-element k step each: the
+// weight ring (packed codes + scales, 18 KB a stage) is deep and is freed by
+// the converters as soon as they have read a stage into registers, so the
+// weight stream from HBM is not held up by the conversion and the MMA; the
+// token ring (the tile's tokens for the k step, mostly L2 hits) is short and
+// is freed by the MMA.
+//
 // Roles (one CTA per SM):
-//   warp 0       TMA producer, per 256-element k stage: the tile's packed
-//                codes (128 rows x 128 bytes, 128-byte swizzle; SwiGLU: 64
-//                gate rows then the 64 up rows of the same features), their
-//                scales (128 rows x 16 bytes), and the tokens (4 k-blocks x
-//                16 or 64 rows x 128 bytes, 128-byte swizzle)
+//   warp 0       TMA producer of the weight ring: the tile's packed codes
+//                (128 rows x 128 bytes, 128-byte swizzle; SwiGLU: 64 gate
+//                rows then the 64 up rows of the same features) and their
+//                scales (128 rows x 16 bytes)
+//   warp 14      TMA producer of the token ring: 4 k-blocks x 16 or 64 rows
+//                x 128 bytes, 128-byte swizzle
 //   warps 6..13  converters, two per TMEM lane quadrant (one per half of
-//                the stage's K): the tokens bf16 -> fp16 in place, and each
-//                thread's weight row (its TMEM lane) e2m1 x e4m3 -> fp16 into
-//                one of three 128-column slots of tensor memory (tcgen05.st)
+//                the stage's K): the tokens bf16 -> fp16 in place (only when
+//                given in bf16), and each thread's weight row (its TMEM lane)
+//                e2m1 x e4m3 -> fp16 into one of three 128-column slots of
+//                tensor memory (tcgen05.st)
 //   warp 1       TMEM allocation; MMA issuer: 16 x tcgen05.mma kind::f16
 //                M=128 N<=64 K=16 per stage, A from the slot, B (tokens) from
-//                shared memory, into one of two 64-column accumulators
+//                shared memory, into one of two accumulators; it starts each
+//                stage on a named-barrier signal from warp 15, which does the
+//                mbarrier waits (slot expanded, tokens landed, accumulator
+//                drained) so that none stalls the issue of the MMAs
 //   warps 2..5   epilogue: accumulator lanes (weight rows) x tokens, scaled
 //                by the weights' fp32 global scale; SwiGLU pairs gate lanes
 //                32q with up lanes 32q+64 through shared memory; 4-byte bf16
@@ -61,7 +73,7 @@ constexpr int CODE_TILE = WM * KS / 2;    // 16 KB of packed E2M1
 constexpr int SF_TILE = WM * KS / 16;     // 2 KB: 16 scale bytes per row
 constexpr int TOK_KBLK = KS / 64;         // 64-element k-blocks of tokens per stage
 constexpr int OFF_SF = CODE_TILE;
-constexpr int OFF_TOK = CODE_TILE + SF_TILE;
+constexpr int W_STAGE = CODE_TILE + SF_TILE;  // 18 KB per weight stage
 constexpr int A_COLS = KS / 2;            // fp16 pairs per row per stage
 constexpr int A_COL0 = 128;               // expanded-weight slots start here
 constexpr int ASLOTS = 3;                 // expanded-weight slots in tensor memory
@@ -74,29 +86,36 @@ constexpr int PART_COLS = A_COLS / KPARTS;       // fp16 pairs a converter threa
 constexpr int PART_CHUNKS = 8 / KPARTS;          // 16-byte code chunks (32 values) per part
 constexpr int PART_SF_WORDS = 4 / KPARTS;        // 32-bit words of scale bytes per part
 constexpr int CONV_THREADS = CONV_WARPS * 32;
-constexpr int NUM_WARPS = 6 + CONV_WARPS;
+constexpr int TOK_WARP = 6 + CONV_WARPS;         // token-ring producer
+constexpr int WAIT_WARP = TOK_WARP + 1;          // waits on behalf of the MMA warp
+constexpr int NUM_WARPS = WAIT_WARP + 1;
+constexpr int MMA_BAR = 3;                       // named barrier: WAIT_WARP -> MMA warp
+static_assert(TOK_WARP == 14 && WAIT_WARP == 15 && NUM_WARPS == 16, "role layout");
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int XCH_FLOATS = 32 * 32;
 constexpr int XCH_BYTES = 2 * 2 * XCH_FLOATS * 4;
-constexpr int EXTRA = (256 + 4 * 2 * (MAX_G + 4) + 15) & ~15;
-static_assert(OFF_TOK % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+constexpr int EXTRA = (512 + 4 * 2 * (MAX_G + 4) + 15) & ~15;
+static_assert(W_STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(A_COL0 + ASLOTS * A_COLS <= TMEM_COLS, "tensor memory budget");
 
 // Two shapes of the same pipeline: TM = 64 tokens per tile (prefill-like
-// launches), and TM = 16 for launches with a few tokens per expert, whose
-// smaller stages (26 KB instead of 50 KB) let 7 stages be in flight instead
-// of 4 while each stage waits on HBM.
+// launches) with 3 token stages and 5 weight stages, and TM = 16 for
+// launches with a few tokens per expert, whose 8 KB token stages leave room
+// for 9 weight stages in flight from HBM.
 template <int TMT>
 struct Cfg {
   static constexpr int TM = TMT;                         // most tokens per tile (N of the MMA)
   static constexpr int TOK_TILE = TMT * KS * 2;
-  static constexpr int STAGE_BYTES = OFF_TOK + TOK_TILE;
-  static constexpr int STAGES = TMT == SMALL_N ? 7 : 4;
+  static constexpr int SW = TMT == SMALL_N ? 9 : 5;      // weight stages
+  static constexpr int ST = TMT == SMALL_N ? 4 : 3;      // token stages
+  static constexpr int OFF_TOKS = SW * W_STAGE;
+  static constexpr int RING_BYTES = OFF_TOKS + ST * TOK_TILE;
   static constexpr int ACC_COLS = TMT;                   // accumulator columns per buffer
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA + XCH_BYTES + 64;
-  static_assert(STAGE_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static constexpr int SMEM = 1024 + RING_BYTES + EXTRA + XCH_BYTES + 64;
+  static_assert(TOK_TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(2 * ACC_COLS <= A_COL0, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(2 * (SW + ST) + 2 * ASLOTS + 5 <= 60, "barrier area");
 };
 
 struct Tile {
@@ -175,26 +194,29 @@ template <int EPI, int TMT>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __grid_constant__ Params p) {
   using C = Cfg<TMT>;
   constexpr int TM = C::TM;
-  constexpr int S = C::STAGES;
-  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int SW = C::SW;
+  constexpr int ST = C::ST;
   constexpr int ACC_COLS = C::ACC_COLS;
   constexpr bool SWIGLU = EPI != MOE_EPI_STORE_BF16;
   constexpr bool OUT_F16 = EPI == kEpiSwigluF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = base;
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + S * STAGE_BYTES);
-  uint64_t* empty = full + S;
-  uint64_t* afull = empty + S;
+  uint8_t* wring = base;                    // weight stages
+  uint8_t* kring = base + C::OFF_TOKS;      // token stages
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(base + C::RING_BYTES);
+  uint64_t* wempty = wfull + SW;
+  uint64_t* kfull = wempty + SW;
+  uint64_t* kempty = kfull + ST;
+  uint64_t* afull = kempty + ST;
   uint64_t* aempty = afull + ASLOTS;
   uint64_t* tfull = aempty + ASLOTS;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* s_prefix = reinterpret_cast<int*>(base + S * STAGE_BYTES + 256);
+  int* s_prefix = reinterpret_cast<int*>(base + C::RING_BYTES + 512);
   int* s_off = s_prefix + MAX_G + 4;
-  float* xch = reinterpret_cast<float*>(base + S * STAGE_BYTES + EXTRA);
+  float* xch = reinterpret_cast<float*>(base + C::RING_BYTES + EXTRA);
   volatile int* pair_ok = reinterpret_cast<volatile int*>(xch + 4 * XCH_FLOATS);
   __shared__ int warp_sums[32];
 
@@ -204,9 +226,13 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
   const int GT = G + (p.shared_rows >= 0 ? 1 : 0);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], CONV_WARPS);
+    }
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1);
     }
     for (int a = 0; a < ASLOTS; ++a) {
       mbar_init(&afull[a], CONV_WARPS);
@@ -232,68 +258,80 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
   const int total = s_prefix[GT];
   const unsigned long long tmo = p.timeout_ns;
 
-  if (warp == 0) {
-    // ===================================================== TMA producer
-    // tma_w: packed codes, tma_wsf: weight scales, tma_a / tma_asf: tokens
-    // with 64-row / 16-row boxes
+  if (warp == 0 || warp == TOK_WARP) {
+    // ===================================================== TMA producers
+    // warp 0: tma_w (packed codes) + tma_wsf (weight scales) into the weight
+    // ring; TOK_WARP: tma_a / tma_asf (tokens, 64-row / 16-row boxes) into
+    // the token ring
     if (lane == 0) {
+      const bool wprod = warp == 0;
+      const int depth = wprod ? SW : ST;
+      uint64_t* fullb = wprod ? wfull : kfull;
+      uint64_t* emptyb = wprod ? wempty : kempty;
       for (int pb = 0; pb < (p.shared_rows >= 0 ? 2 : 1); ++pb) {
-        tma_prefetch_desc(&p.tma_a[pb]);
-        tma_prefetch_desc(&p.tma_asf[pb]);
-        tma_prefetch_desc(&p.tma_w[pb]);
-        tma_prefetch_desc(&p.tma_wsf[pb]);
+        if (wprod) {
+          tma_prefetch_desc(&p.tma_w[pb]);
+          tma_prefetch_desc(&p.tma_wsf[pb]);
+        } else {
+          tma_prefetch_desc(&p.tma_a[pb]);
+          tma_prefetch_desc(&p.tma_asf[pb]);
+        }
       }
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued[S];
+      uint32_t issued[SW];
 #pragma unroll
-      for (int s = 0; s < S; ++s) issued[s] = 0;
+      for (int s = 0; s < SW; ++s) issued[s] = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
         const Prob& P = p.prob[ti.pb];
         const bool small = ti.n <= SMALL_N;
         const void* tt = small ? &p.tma_asf[ti.pb] : &p.tma_a[ti.pb];
-        const uint32_t tx = static_cast<uint32_t>(CODE_TILE + SF_TILE + TOK_KBLK * (small ? SMALL_N : TM) * 128);
+        const uint32_t tx = wprod ? static_cast<uint32_t>(W_STAGE)
+                                  : static_cast<uint32_t>(TOK_KBLK * (small ? SMALL_N : TM) * 128);
         const int f0 = ti.blk * (WM / 2);                  // SwiGLU: 64 features
         const int w_y = ti.g * P.w_rows + ti.blk * WM;     // STORE: 128 weight rows
         const int nk = P.K / KS;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, tmo, p.err, abort_flag)) {
+          if (!mbar_wait_bounded(&emptyb[stage], phase ^ 1u, tmo, p.err, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t* sb = stages + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], tx);
-          if (SWIGLU) {
-            tma_load_3d(&p.tma_w[ti.pb], &full[stage], sb, kb * (KS / 2), f0, 2 * ti.g);
-            tma_load_3d(&p.tma_wsf[ti.pb], &full[stage], sb + OFF_SF, kb * (KS / 16), f0, 2 * ti.g);
+          mbar_arrive_expect_tx(&fullb[stage], tx);
+          if (wprod) {
+            uint8_t* sb = wring + stage * W_STAGE;
+            if (SWIGLU) {
+              tma_load_3d(&p.tma_w[ti.pb], &fullb[stage], sb, kb * (KS / 2), f0, 2 * ti.g);
+              tma_load_3d(&p.tma_wsf[ti.pb], &fullb[stage], sb + OFF_SF, kb * (KS / 16), f0, 2 * ti.g);
+            } else {
+              tma_load_2d(&p.tma_w[ti.pb], &fullb[stage], sb, kb * (KS / 2), w_y);
+              tma_load_2d(&p.tma_wsf[ti.pb], &fullb[stage], sb + OFF_SF, kb * (KS / 16), w_y);
+            }
           } else {
-            tma_load_2d(&p.tma_w[ti.pb], &full[stage], sb, kb * (KS / 2), w_y);
-            tma_load_2d(&p.tma_wsf[ti.pb], &full[stage], sb + OFF_SF, kb * (KS / 16), w_y);
+            tma_load_3d(tt, &fullb[stage], kring + stage * C::TOK_TILE, 0, ti.row0, kb * TOK_KBLK);
           }
-          tma_load_3d(tt, &full[stage], sb + OFF_TOK, 0, ti.row0, kb * TOK_KBLK);
           issued[stage] += 1;
-          if (++stage == S) {
+          if (++stage == depth) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < S; ++s)
-          if (issued[s]) mbar_wait_bounded(&full[s], (issued[s] - 1u) & 1u, 1000000000ull, p.err, nullptr);
+        for (int s = 0; s < depth; ++s)
+          if (issued[s]) mbar_wait_bounded(&fullb[s], (issued[s] - 1u) & 1u, 1000000000ull, p.err, nullptr);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 6 + CONV_WARPS) {
     // ===================================================== converters
     const int cw = warp - 6;
     const int ctid = cw * 32 + lane;
     const int q = warp & 3;          // TMEM lane quadrant
     const int kh = cw >> 2;          // part of the stage's K this warp expands
     const int row = q * 32 + lane;   // weight row of the tile = TMEM lane
-    int stage = 0, slot = 0;
-    uint32_t phase = 0, sphase = 0;
+    int ws = 0, ks = 0, slot = 0;
+    uint32_t wphase = 0, kphase = 0, sphase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
@@ -302,39 +340,60 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
       // 16-byte chunks of the token rows the MMA reads, when given in bf16
       const int tok_chunks = p.prob[ti.pb].a_f16 ? 0 : TOK_KBLK * ti.n * 8;
       for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait_warp(&full[stage], phase, tmo, p.err, abort_flag) ||
-            !mbar_wait_warp(&aempty[slot], sphase ^ 1u, tmo, p.err, abort_flag)) {
+        if (!mbar_wait_warp(&wfull[ws], wphase, tmo, p.err, abort_flag)) {
           ok = false;
           break;
         }
-        uint8_t* sb = stages + stage * STAGE_BYTES;
-        // tokens: bf16 -> fp16 in place (the swizzle moves whole 16-byte chunks)
-        for (int c = ctid; c < tok_chunks; c += CONV_THREADS) {
-          const int kblk = c / (ti.n * 8);
-          const int rem = c - kblk * ti.n * 8;
-          uint4* ptr = reinterpret_cast<uint4*>(sb + OFF_TOK + kblk * kstride + rem * 16);
-          uint4 v = *ptr;
-          v.x = bf16x2_to_f16x2_sat(v.x);
-          v.y = bf16x2_to_f16x2_sat(v.y);
-          v.z = bf16x2_to_f16x2_sat(v.z);
-          v.w = bf16x2_to_f16x2_sat(v.w);
-          *ptr = v;
-        }
-        // weights: this thread's row, elements [kh*256/KPARTS, +256/KPARTS) of the stage
-        const uint8_t* crow = sb + row * 128;
+        // this thread's row, elements [kh*256/KPARTS, +256/KPARTS) of the stage,
+        // into registers; then the weight stage is free for the next copy
+        const uint8_t* wsb = wring + ws * W_STAGE;
+        const uint8_t* crow = wsb + row * 128;
         uint32_t sw[PART_SF_WORDS];
 #pragma unroll
         for (int i = 0; i < PART_SF_WORDS; ++i)
-          sw[i] = *reinterpret_cast<const uint32_t*>(sb + OFF_SF + row * 16 + kh * 4 * PART_SF_WORDS + 4 * i);
-        uint32_t r[PART_COLS];
+          sw[i] = *reinterpret_cast<const uint32_t*>(wsb + OFF_SF + row * 16 + kh * 4 * PART_SF_WORDS + 4 * i);
+        uint4 cv[PART_CHUNKS];
 #pragma unroll
         for (int c4 = 0; c4 < PART_CHUNKS; ++c4) {
           const int j = PART_CHUNKS * kh + c4;  // 16-byte chunk of the row (32 elements, two scale blocks)
-          const uint4 cv = *reinterpret_cast<const uint4*>(crow + ((j ^ (row & 7)) << 4));
+          cv[c4] = *reinterpret_cast<const uint4*>(crow + ((j ^ (row & 7)) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty[ws]);
+        if (++ws == SW) {
+          ws = 0;
+          wphase ^= 1u;
+        }
+        if (tok_chunks) {
+          // tokens: bf16 -> fp16 in place (the swizzle moves whole 16-byte chunks)
+          if (!mbar_wait_warp(&kfull[ks], kphase, tmo, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* ksb = kring + ks * C::TOK_TILE;
+          for (int c = ctid; c < tok_chunks; c += CONV_THREADS) {
+            const int kblk = c / (ti.n * 8);
+            const int rem = c - kblk * ti.n * 8;
+            uint4* ptr = reinterpret_cast<uint4*>(ksb + kblk * kstride + rem * 16);
+            uint4 v = *ptr;
+            v.x = bf16x2_to_f16x2_sat(v.x);
+            v.y = bf16x2_to_f16x2_sat(v.y);
+            v.z = bf16x2_to_f16x2_sat(v.z);
+            v.w = bf16x2_to_f16x2_sat(v.w);
+            *ptr = v;
+          }
+        }
+        if (++ks == ST) {
+          ks = 0;
+          kphase ^= 1u;
+        }
+        uint32_t r[PART_COLS];
+#pragma unroll
+        for (int c4 = 0; c4 < PART_CHUNKS; ++c4) {
           const uint32_t sbytes = (sw[c4 >> 1] >> (16 * (c4 & 1))) & 0xFFFFu;
           const uint32_t s2 = e4m3x2_to_f16x2(sbytes);
           const uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
-          const uint32_t words[4] = {cv.x, cv.y, cv.z, cv.w};
+          const uint32_t words[4] = {cv[c4].x, cv[c4].y, cv[c4].z, cv[c4].w};
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
             const uint32_t sc = wi < 2 ? s_lo : s_hi;
@@ -348,18 +407,18 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
             for (int bi = 0; bi < 4; ++bi) r[c4 * 16 + wi * 4 + bi] = hmul2_u32(o[bi], sc);
           }
         }
+        if (!mbar_wait_warp(&aempty[slot], sphase ^ 1u, tmo, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
         const uint32_t a_dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(A_COL0 + slot * A_COLS + kh * PART_COLS);
         tmem_st_part(a_dst, r);
         tmem_st_wait();
-        fence_proxy_async_smem();  // the converted tokens are read by the MMA (async proxy)
+        if (tok_chunks) fence_proxy_async_smem();  // the converted tokens are read by the MMA (async proxy)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&afull[slot]);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
         if (++slot == ASLOTS) {
           slot = 0;
           sphase ^= 1u;
@@ -368,53 +427,72 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
     }
   } else if (warp == 1) {
     // ===================================================== MMA issuer
-    if (lane == 0) {
-      int stage = 0, slot = 0;
-      uint32_t phase = 0, sphase = 0;
-      bool ok = true;
-      int it = 0;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
-        const int nk = p.prob[ti.pb].K / KS;
-        const uint32_t idesc = idesc_f16_f32(WM, ti.n);
-        const uint32_t kstride = static_cast<uint32_t>((ti.n <= SMALL_N ? SMALL_N : TM) * 128);
-        const int buf = it & 1;
-        const uint32_t use = static_cast<uint32_t>(it >> 1);
-        if (!mbar_wait_bounded(&tempty[buf], (use & 1u) ^ 1u, tmo, p.err, abort_flag)) {
+    // The whole warp walks the schedule and issues (elect.sync picks the
+    // lane, the code stays converged).  Each stage starts on
+    // the go signal of WAIT_WARP (slot expanded, token stage landed and, on
+    // a tile's first stage, the accumulator drained), so this warp itself
+    // never waits on an mbarrier between its MMAs.
+    const uint64_t tok_desc0 = smem_desc_kmajor_sw128(smem_u32(kring));
+    int ks = 0, slot = 0;
+    bool ok = true;
+    int it = 0;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+      const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const int nk = p.prob[ti.pb].K / KS;
+      const uint32_t idesc = idesc_f16_f32(WM, ti.n);
+      const uint32_t kstride16 = static_cast<uint32_t>((ti.n <= SMALL_N ? SMALL_N : TM) * 128) >> 4;
+      const uint32_t d = tmem_base + static_cast<uint32_t>((it & 1) * ACC_COLS);
+      for (int kb = 0; kb < nk; ++kb) {
+        if (named_bar_red_or(MMA_BAR, 64, false)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * ACC_COLS);
-        for (int kb = 0; kb < nk; ++kb) {
-          // the converters saw the stage land (full) before they filled the slot
-          if (!mbar_wait_bounded(&afull[slot], sphase, tmo, p.err, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t tok = smem_u32(stages + stage * STAGE_BYTES + OFF_TOK);
-          const uint32_t a0 = tmem_base + static_cast<uint32_t>(A_COL0 + slot * A_COLS);
+        const uint64_t db = tok_desc0 + static_cast<uint64_t>((ks * C::TOK_TILE) >> 4);
+        const uint32_t a0 = tmem_base + static_cast<uint32_t>(A_COL0 + slot * A_COLS);
+        umma_f16_ts_warp(d, a0, db, idesc, kb ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < KS / 16; ++kk)
-            umma_f16_ts(d, a0 + 8 * kk, smem_desc_kmajor_sw128(tok + (kk >> 2) * kstride + (kk & 3) * 32), idesc,
-                        (kb | kk) ? 1u : 0u);
-          umma_commit(&empty[stage]);
-          umma_commit(&aempty[slot]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (++slot == ASLOTS) {
-            slot = 0;
-            sphase ^= 1u;
-          }
-        }
-        if (ok) umma_commit(&tfull[buf]);
+        for (int kk = 1; kk < KS / 16; ++kk)
+          umma_f16_ts_warp(d, a0 + 8 * kk, db + static_cast<uint64_t>((kk >> 2) * kstride16 + (kk & 3) * 2), idesc, 1u);
+        umma_commit_warp(&kempty[ks]);
+        umma_commit_warp(&aempty[slot]);
+        if (++ks == ST) ks = 0;
+        if (++slot == ASLOTS) slot = 0;
       }
-      if (!ok) {
-        umma_commit(drain);
-        mbar_wait_bounded(drain, 0, 1000000000ull, p.err, nullptr);
+      if (ok) umma_commit_warp(&tfull[it & 1]);
+    }
+    if (!ok && lane == 0) {
+      umma_commit(drain);
+      mbar_wait_bounded(drain, 0, 1000000000ull, p.err, nullptr);
+    }
+  } else if (warp == WAIT_WARP) {
+    // ===================================================== waits for the MMA warp
+    int ks = 0, slot = 0;
+    uint32_t kphase = 0, sphase = 0;
+    bool ok = true;
+    int it = 0;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+      const Tile ti = decode_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const int nk = p.prob[ti.pb].K / KS;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      for (int kb = 0; kb < nk; ++kb) {
+        // afull: the slot is expanded (and, for bf16 tokens, the token stage
+        // converted); kfull: the token stage has landed
+        bool good = (kb > 0 || mbar_wait_warp(&tempty[it & 1], (use & 1u) ^ 1u, tmo, p.err, abort_flag)) &&
+                    mbar_wait_warp(&afull[slot], sphase, tmo, p.err, abort_flag) &&
+                    mbar_wait_warp(&kfull[ks], kphase, tmo, p.err, abort_flag);
+        if (named_bar_red_or(MMA_BAR, 64, !good)) {
+          ok = false;
+          break;
+        }
+        if (++ks == ST) {
+          ks = 0;
+          kphase ^= 1u;
+        }
+        if (++slot == ASLOTS) {
+          slot = 0;
+          sphase ^= 1u;
+        }
       }
     }
   } else {
