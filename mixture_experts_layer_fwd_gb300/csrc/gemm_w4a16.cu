@@ -74,9 +74,8 @@ constexpr int SF_TILE = WM * KS / 16;     // 2 KB: 16 scale bytes per row
 constexpr int TOK_KBLK = KS / 64;         // 64-element k-blocks of tokens per stage
 constexpr int OFF_SF = CODE_TILE;
 constexpr int W_STAGE = CODE_TILE + SF_TILE;  // 18 KB per weight stage
-constexpr int A_COLS = KS / 2;            // fp16 pairs per row per stage
-constexpr int A_COL0 = 128;               // expanded-weight slots start here
-constexpr int ASLOTS = 3;                 // expanded-weight slots in tensor memory
+constexpr int A_COLS = KS / 2;            // fp16 pairs per row per stage = TMEM columns per slot
+constexpr int MAX_ASLOTS = 3;             // expanded-weight slots in tensor memory (at most)
 constexpr int TMEM_COLS = 512;
 // 4 lane quadrants x KPARTS parts of the stage's K (16 warps measured slower:
 // the register cap of a 704-thread block spills the epilogue)
@@ -96,26 +95,31 @@ constexpr int XCH_FLOATS = 32 * 32;
 constexpr int XCH_BYTES = 2 * 2 * XCH_FLOATS * 4;
 constexpr int EXTRA = (512 + 4 * 2 * (MAX_G + 4) + 15) & ~15;
 static_assert(W_STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-static_assert(A_COL0 + ASLOTS * A_COLS <= TMEM_COLS, "tensor memory budget");
+static_assert(PART_COLS == 64, "a converter thread stores its part as two 32-column halves");
 
-// Two shapes of the same pipeline: TM = 64 tokens per tile (prefill-like
-// launches) with 3 token stages and 5 weight stages, and TM = 16 for
-// launches with a few tokens per expert, whose 8 KB token stages leave room
-// for 9 weight stages in flight from HBM.
+// Three shapes of the same pipeline: TM = 16 for launches with a few tokens
+// per expert, whose 8 KB token stages leave room for 9 weight stages in
+// flight from HBM; TM = 64 with 3 token stages and 5 weight stages; and
+// TM = 128 for launches averaging more than 48 rows per expert, so that a
+// weight tile is expanded once for up to 128 tokens (two 128-column
+// accumulators leave tensor memory for two expanded-weight slots).
 template <int TMT>
 struct Cfg {
   static constexpr int TM = TMT;                         // most tokens per tile (N of the MMA)
   static constexpr int TOK_TILE = TMT * KS * 2;
-  static constexpr int SW = TMT == SMALL_N ? 9 : 5;      // weight stages
-  static constexpr int ST = TMT == SMALL_N ? 4 : 3;      // token stages
+  static constexpr int SW = TMT == SMALL_N ? 9 : (TMT == 64 ? 5 : 4);   // weight stages
+  static constexpr int ST = TMT == SMALL_N ? 4 : (TMT == 64 ? 3 : 2);   // token stages
+  static constexpr int ASLOTS = TMT == 128 ? 2 : 3;      // expanded-weight slots
+  static constexpr int A_COL0 = TMT == 128 ? 256 : 128;  // first slot column (accumulators below)
   static constexpr int OFF_TOKS = SW * W_STAGE;
   static constexpr int RING_BYTES = OFF_TOKS + ST * TOK_TILE;
   static constexpr int ACC_COLS = TMT;                   // accumulator columns per buffer
   static constexpr int SMEM = 1024 + RING_BYTES + EXTRA + XCH_BYTES + 64;
   static_assert(TOK_TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  static_assert(2 * ACC_COLS <= A_COL0, "tensor memory budget");
+  static_assert(2 * ACC_COLS <= A_COL0 && A_COL0 + ASLOTS * A_COLS <= TMEM_COLS, "tensor memory budget");
+  static_assert(ASLOTS <= MAX_ASLOTS, "barrier arrays");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(2 * (SW + ST) + 2 * ASLOTS + 5 <= 60, "barrier area");
+  static_assert(2 * (SW + ST) + 2 * MAX_ASLOTS + 5 <= 60, "barrier area");
 };
 
 struct Tile {
@@ -154,8 +158,6 @@ DEVINL uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
   return r;
 }
 
-DEVINL void tmem_st_part(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st_32x32b_x64(taddr, r); }
-DEVINL void tmem_st_part(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st_32x32b_x32(taddr, r); }
 
 DEVINL uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -197,6 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
   constexpr int SW = C::SW;
   constexpr int ST = C::ST;
   constexpr int ACC_COLS = C::ACC_COLS;
+  constexpr int ASLOTS = C::ASLOTS;
+  constexpr int A_COL0 = C::A_COL0;
   constexpr bool SWIGLU = EPI != MOE_EPI_STORE_BF16;
   constexpr bool OUT_F16 = EPI == kEpiSwigluF16;
   extern __shared__ uint8_t smem_raw[];
@@ -208,8 +212,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
   uint64_t* kfull = wempty + SW;
   uint64_t* kempty = kfull + ST;
   uint64_t* afull = kempty + ST;
-  uint64_t* aempty = afull + ASLOTS;
-  uint64_t* tfull = aempty + ASLOTS;
+  uint64_t* aempty = afull + MAX_ASLOTS;
+  uint64_t* tfull = aempty + MAX_ASLOTS;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -387,9 +391,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
           ks = 0;
           kphase ^= 1u;
         }
-        uint32_t r[PART_COLS];
-#pragma unroll
-        for (int c4 = 0; c4 < PART_CHUNKS; ++c4) {
+        const uint32_t a_dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(A_COL0 + slot * A_COLS + kh * PART_COLS);
+        auto conv = [&](int c4, uint32_t* rr) {
           const uint32_t sbytes = (sw[c4 >> 1] >> (16 * (c4 & 1))) & 0xFFFFu;
           const uint32_t s2 = e4m3x2_to_f16x2(sbytes);
           const uint32_t s_lo = __byte_perm(s2, 0, 0x1010), s_hi = __byte_perm(s2, 0, 0x3232);
@@ -404,17 +408,26 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_w4a16_kernel(const __
                 : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
                 : "r"(words[wi]));
 #pragma unroll
-            for (int bi = 0; bi < 4; ++bi) r[c4 * 16 + wi * 4 + bi] = hmul2_u32(o[bi], sc);
+            for (int bi = 0; bi < 4; ++bi) rr[wi * 4 + bi] = hmul2_u32(o[bi], sc);
           }
+        };
+        // first half of the row: expand, wait for the slot, store; the
+        // second half is expanded while the first store is in flight
+        {
+          uint32_t r[PART_COLS / 2];
+#pragma unroll
+          for (int c4 = 0; c4 < PART_CHUNKS / 2; ++c4) conv(c4, r + c4 * 16);
+          if (!mbar_wait_warp(&aempty[slot], sphase ^ 1u, tmo, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tmem_st_32x32b_x32(a_dst, r);
+          uint32_t r2[PART_COLS / 2];
+#pragma unroll
+          for (int c4 = 0; c4 < PART_CHUNKS / 2; ++c4) conv(PART_CHUNKS / 2 + c4, r2 + c4 * 16);
+          tmem_st_32x32b_x32(a_dst + PART_COLS / 2, r2);
+          tmem_st_wait();
         }
-        if (!mbar_wait_warp(&aempty[slot], sphase ^ 1u, tmo, p.err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t a_dst = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(A_COL0 + slot * A_COLS + kh * PART_COLS);
-        tmem_st_part(a_dst, r);
-        tmem_st_wait();
         if (tok_chunks) fence_proxy_async_smem();  // the converted tokens are read by the MMA (async proxy)
         tc_fence_before();
         __syncwarp();
@@ -603,8 +616,10 @@ static int launch(const Params& prm, cudaStream_t s) {
 }
 
 template <int EPI>
-static int launch_shape(const Params& prm, bool small, cudaStream_t s) {
-  return small ? launch<EPI, SMALL_N>(prm, s) : launch<EPI, 64>(prm, s);
+static int launch_shape(const Params& prm, int tm, cudaStream_t s) {
+  if (tm == SMALL_N) return launch<EPI, SMALL_N>(prm, s);
+  if (tm == 64) return launch<EPI, 64>(prm, s);
+  return launch<EPI, 128>(prm, s);
 }
 
 static int fill(Params& prm, int slot, int epi, const GemmProblem& P, int tm) {
@@ -662,9 +677,11 @@ int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t*
   memset(&prm, 0, sizeof(prm));
   // a few routed rows per expert (decode): 16-token tiles and a deeper
   // pipeline; from ~10 rows per expert on, splitting the busier groups into
-  // 16-token tiles re-expands their weights more often than it gains
-  const bool small = static_cast<long long>(routed.a_rows) <= 4ll * G;
-  const int tm = small ? gw4::SMALL_N : 64;
+  // 16-token tiles re-expands their weights more often than it gains; past
+  // 48 rows per expert on average, 128-token tiles expand each weight tile
+  // once for most groups
+  const long long rows = routed.a_rows;
+  const int tm = rows <= 4ll * G ? gw4::SMALL_N : (rows > 48ll * G ? 128 : 64);
   MOE_TRY(gw4::fill(prm, 0, epi, routed, tm));
   prm.offsets = offsets;
   prm.G = G;
@@ -676,9 +693,9 @@ int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t*
   prm.err = device_error_word();
   if (!prm.err) return MOE_ERR_CUDA;
   prm.timeout_ns = wait_timeout_ns();
-  if (epi == MOE_EPI_STORE_BF16) return gw4::launch_shape<MOE_EPI_STORE_BF16>(prm, small, s);
-  if (epi == kEpiSwigluF16) return gw4::launch_shape<kEpiSwigluF16>(prm, small, s);
-  return gw4::launch_shape<MOE_EPI_SWIGLU_BF16>(prm, small, s);
+  if (epi == MOE_EPI_STORE_BF16) return gw4::launch_shape<MOE_EPI_STORE_BF16>(prm, tm, s);
+  if (epi == kEpiSwigluF16) return gw4::launch_shape<kEpiSwigluF16>(prm, tm, s);
+  return gw4::launch_shape<MOE_EPI_SWIGLU_BF16>(prm, tm, s);
 }
 
 }  // namespace moe

@@ -271,15 +271,23 @@ def test_grouped_gemm_bf16_token_blocks(epi):
     assert row_err.max() < 2e-2, int(row_err.argmax())
 
 
-@pytest.mark.parametrize("epi,N,K,few", [(1, 256, 512, False), (0, 384, 768, False), (1, 192, 320, False),
-                                         (0, 128, 576, False), (1, 256, 1024, True), (0, 512, 256, True)])
-def test_grouped_gemm_nvfp4_weights(epi, N, K, few):
+W4A16_COUNTS = {
+    "few": [1, 2, 0, 20, 3, 2, 1, 0, 5, 1],        # <= 4 rows per group on average: 16-token tiles
+    "mid": [3, 40, 0, 70, 9, 17, 1, 30],           # 5..48 rows per group: 64-token tiles
+    "many": [3, 200, 0, 64, 129, 17],              # > 48 rows per group: 128-token tiles
+}
+
+
+@pytest.mark.parametrize("epi,N,K,rows", [(1, 256, 512, "many"), (0, 384, 768, "many"), (1, 192, 320, "many"),
+                                          (0, 128, 576, "many"), (1, 256, 1024, "few"), (0, 512, 256, "few"),
+                                          (1, 384, 512, "mid"), (0, 256, 768, "mid")])
+def test_grouped_gemm_nvfp4_weights(epi, N, K, rows):
     """bf16 A x NVFP4 W (codes + E4M3 scales + per-group fp32 scale): K a
-    multiple of 256 (weights expanded into tensor memory, fp16 MMA; 64-token
-    tiles, or 16-token tiles when the groups average <= 4 rows) and not
+    multiple of 256 (weights expanded into tensor memory, fp16 MMA, in each
+    of the three token-tile shapes, chosen by the rows per group) and not
     (converter kernel, bf16 MMA); ragged groups past a tile and empty ones."""
     m = api()
-    counts = [1, 2, 0, 20, 3, 2, 1, 0, 5, 1] if few else [3, 200, 0, 64, 129, 17]
+    counts = W4A16_COUNTS[rows]
     offs = _ragged_offsets(counts)
     M, G = int(offs[-1]), len(counts)
     Wn = 2 * N if epi == 1 else N
