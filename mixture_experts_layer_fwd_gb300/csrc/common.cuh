@@ -316,6 +316,29 @@ DEVINL uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 DEVINL void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrive on a barrier of the peer CTA without a cluster-scope release, for
+// signals that publish only tensor-memory state: tensor-memory stores
+// completed by tcgen05.wait::st, or an accumulator fully read
+// (tcgen05.wait::ld), ordered by tcgen05.fence::before_thread_sync.  A
+// release at cluster scope fences every outstanding memory operation of the
+// thread (on GB300 it cost the NVFP4 pair GEMM 1.7x its time when done per
+// k step).
+DEVINL void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Phase test without acquire, for barriers whose arrivals publish only
+// tensor-memory state or TMA data (followed by tcgen05.fence::after_thread_sync).
+DEVINL bool mbar_try_wait_relaxed_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

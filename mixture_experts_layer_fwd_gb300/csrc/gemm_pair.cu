@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
         // both CTAs' epilogues must have drained this accumulator buffer
         {
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait_cluster(&tempty[buf], (use & 1u) ^ 1u)) {
+          while (!mbar_try_wait_relaxed_cluster(&tempty[buf], (use & 1u) ^ 1u)) {
             if (*abort_flag || globaltimer_ns() - t0 > tmo) {
               atomicOr(p.err, kErrTimeout);
               *abort_flag = 1;
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
         if (leader)
           mbar_arrive(&tempty[buf]);
         else
-          mbar_arrive_remote(tempty_leader + static_cast<uint32_t>(buf) * 8u);
+          mbar_arrive_remote_relaxed(tempty_leader + static_cast<uint32_t>(buf) * 8u);
       }
     }
   }

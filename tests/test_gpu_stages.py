@@ -331,6 +331,66 @@ def test_grouped_gemm_nvfp4_both_block_scaled(epi, N, K):
     assert err < 5e-3, err
 
 
+@pytest.mark.parametrize("epi,N,K", [(0, 448, 512), (1, 256, 768), (0, 192, 256), (1, 192, 1280)])
+def test_grouped_gemm_nvfp4_both_large_groups(epi, N, K):
+    """NVFP4 A x NVFP4 W with prefill-sized groups (>= 192 rows per group on
+    average): groups past one and two 256-row blocks, a ragged last weight
+    tile (N = 448, SwiGLU N = 256), empty groups and a group of 64 rows."""
+    m = api()
+    counts = [300, 0, 513, 257, 64, 130]
+    offs = _ragged_offsets(counts)
+    M, G = int(offs[-1]), len(counts)
+    assert M >= 192 * G
+    Wn = N if epi == 0 else 2 * N
+    g = torch.Generator().manual_seed(N + K + 3 * epi)
+    Aq, As, Ag = nvfp4.quantize(torch.randn(M, K, generator=g).numpy())
+    Wq = [nvfp4.quantize((torch.randn(Wn, K, generator=g) * 0.02).numpy()) for _ in range(G)]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    C = m.moe_grouped_gemm(1, 1, epi, offs.to(DEV), N, K, t(Aq), t(np.stack([q for q, _, _ in Wq])), A_sf=t(As),
+                           A_g=torch.tensor([Ag], device=DEV), W_sf=t(np.stack([s for _, s, _ in Wq])),
+                           W_g=torch.tensor([gg for _, _, gg in Wq], dtype=torch.float32, device=DEV))
+    _sync()
+    Ad = nvfp4.dequantize(Aq, As, Ag)
+    Wd = np.stack([nvfp4.dequantize(q, s, gg) for q, s, gg in Wq])
+    ref = _gemm_ref(Ad, Wd, offs.numpy(), epi == 1, N)
+    got = C.float().cpu().numpy()
+    err = oracle.rel_frobenius(got, ref)
+    assert err < 5e-3, err
+    # every row is written: no row keeps the allocation's contents
+    row_err = np.abs(got - ref).max(axis=1) / (np.abs(ref).max() + 1e-30)
+    assert row_err.max() < 2e-2, int(row_err.argmax())
+
+
+def test_grouped_gemm_nvfp4_both_large_groups_nvfp4_output():
+    """Prefill-sized groups with the SwiGLU output quantised to NVFP4 (N =
+    352 features: a last 64-column weight tile that is half empty)."""
+    m = api()
+    counts = [260, 400, 0, 330]
+    offs = _ragged_offsets(counts)
+    M, G, N, K = int(offs[-1]), len(counts), 352, 512
+    assert M >= 192 * G
+    g = torch.Generator().manual_seed(23)
+    Aq, As, Ag = nvfp4.quantize(torch.randn(M, K, generator=g).numpy())
+    Wq = [nvfp4.quantize((torch.randn(2 * N, K, generator=g) * 0.02).numpy()) for _ in range(G)]
+    gh = F32(8.0 / 2688)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    C, C_sf = m.moe_grouped_gemm(
+        1, 1, 2, offs.to(DEV), N, K, t(Aq), t(np.stack([q for q, _, _ in Wq])), A_sf=t(As),
+        A_g=torch.tensor([Ag], device=DEV), W_sf=t(np.stack([s for _, s, _ in Wq])),
+        W_g=torch.tensor([gg for _, _, gg in Wq], dtype=torch.float32, device=DEV),
+        c_g=torch.tensor([gh], device=DEV))
+    _sync()
+    Ad = nvfp4.dequantize(Aq, As, Ag)
+    Wd = np.stack([nvfp4.dequantize(q, s, gg) for q, s, gg in Wq])
+    h = _gemm_ref(Ad, Wd, offs.numpy(), True, N)
+    rq, rs, _ = nvfp4.quantize(h.astype(F32), gh)
+    got_q, got_s = C.cpu().numpy(), C_sf.cpu().numpy()
+    assert np.mean(got_s != rs) < 1e-3
+    assert np.mean(nvfp4.unpack_codes(got_q) != nvfp4.unpack_codes(rq)) < 2e-3
+    err = oracle.rel_frobenius(nvfp4.dequantize(got_q, got_s, gh), nvfp4.dequantize(rq, rs, gh))
+    assert err < 1e-2, err
+
+
 def test_grouped_gemm_nvfp4_both_with_nvfp4_output():
     """NVFP4 A x NVFP4 W, SwiGLU output quantised to NVFP4 with a given scale."""
     m = api()
