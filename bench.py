@@ -222,12 +222,15 @@ def gemm_work(cfg, T, active_experts):
 
 
 def gemm_kernel_name(cfg):
-    """The grouped-GEMM kernel a layer's formats dispatch to."""
+    """The grouped-GEMM kernel a layer's formats and shapes dispatch to (the
+    NVFP4 kernels with 256-element k stages need every reduction length, H
+    and I, to be a multiple of 256)."""
     if cfg.w_fmt == "bf16" and cfg.act_fmt == "bf16":
         return "grouped_gemm_pair_kernel"
+    k256 = cfg.H % 256 == 0 and cfg.I % 256 == 0 and cfg.I_s % 256 == 0
     if cfg.w_fmt == "nvfp4" and cfg.act_fmt == "nvfp4":
-        return "grouped_gemm_nvf4_kernel"
-    return "grouped_gemm_kernel"
+        return "grouped_gemm_nvf4w_kernel" if k256 else "grouped_gemm_nvf4_kernel"
+    return "grouped_gemm_w4a16_kernel" if k256 else "grouped_gemm_kernel"
 
 
 def tensor_peak(cfg, p):

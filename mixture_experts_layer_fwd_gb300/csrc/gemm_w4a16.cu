@@ -19,9 +19,9 @@
 //
 // Tiles: weights on the MMA's M side (128 weight rows), tokens on N (a group
 // of r routed rows is cut into ceil(r/TM) equal token blocks rounded up to
-// 16; TM = 64, or 16 when the launch averages at most 4 routed rows per
-// expert), so a weight tile is expanded once per TM tokens and a decode step
-// (a few tokens per expert) streams each weight once.
+// 16; TM = 16 when the launch averages at most 4 routed rows per expert, 128
+// past 48, else 64), so a weight tile is expanded once per TM tokens and a
+// decode step (a few tokens per expert) streams each weight once.
 //
 // Two rings of shared-memory stages, one per 256-element k step each: the
 // weight ring (packed codes + scales, 18 KB a stage) is deep and is freed by
@@ -35,16 +35,18 @@
 //                (128 rows x 128 bytes, 128-byte swizzle; SwiGLU: 64 gate
 //                rows then the 64 up rows of the same features) and their
 //                scales (128 rows x 16 bytes)
-//   warp 14      TMA producer of the token ring: 4 k-blocks x 16 or 64 rows
-//                x 128 bytes, 128-byte swizzle
+//   warp 14      TMA producer of the token ring: 4 k-blocks x 16, 64 or 128
+//                rows x 128 bytes, 128-byte swizzle
 //   warps 6..13  converters, two per TMEM lane quadrant (one per half of
 //                the stage's K): the tokens bf16 -> fp16 in place (only when
 //                given in bf16), and each thread's weight row (its TMEM lane)
-//                e2m1 x e4m3 -> fp16 into one of three 128-column slots of
-//                tensor memory (tcgen05.st)
+//                e2m1 x e4m3 -> fp16 into one of the (two or three)
+//                128-column slots of tensor memory (tcgen05.st; the first
+//                half of the row is stored while the second is expanded)
 //   warp 1       TMEM allocation; MMA issuer: 16 x tcgen05.mma kind::f16
-//                M=128 N<=64 K=16 per stage, A from the slot, B (tokens) from
-//                shared memory, into one of two accumulators; it starts each
+//                M=128 N<=128 K=16 per stage, A from the slot, B (tokens)
+//                from shared memory, into one of two accumulators, issued by
+//                the converged warp (elect.sync picks the lane); it starts each
 //                stage on a named-barrier signal from warp 15, which does the
 //                mbarrier waits (slot expanded, tokens landed, accumulator
 //                drained) so that none stalls the issue of the MMAs
