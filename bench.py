@@ -186,7 +186,7 @@ def workload(args):
     if args.workload == "small":
         return SMALL_CFG, T_SMALL
     if args.config is None:
-        return CFG, (args.T or T_MAIN)
+        return CFG, (CFG.E // CFG.k if args.forced else (args.T or T_MAIN))
     if args.config == "deepseek-v3-sweep":
         cfg = synth.sweep_config(args.w_fmt or "nvfp4", args.zipf if args.zipf is not None else 1.1)
     else:
@@ -194,6 +194,10 @@ def workload(args):
         if args.zipf is not None:
             cfg = dataclasses.replace(cfg, zipf=args.zipf)
     T = args.T or max(cfg.Ts)
+    if args.forced:
+        if cfg.E % cfg.k:
+            raise SystemExit(f"--forced needs E % k == 0 ({cfg.name}: E={cfg.E}, k={cfg.k})")
+        T = cfg.E // cfg.k  # every expert receives exactly one token
     if args.experts:
         # profiling variant: fewer experts, same tokens per expert (T*k/E)
         T = max(1, T * args.experts // cfg.E)
@@ -345,8 +349,12 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     _build.build()
     cfg, T = workload(args)
-    is_main = args.workload == "main" and args.config is None and T == T_MAIN
+    is_main = args.workload == "main" and args.config is None and T == T_MAIN and not args.forced
     acts = synth.make_activations(cfg, T, seed=0)
+    if args.forced:
+        # the decode microbenchmark shape: all experts active, one token each
+        _, forced_logits = synth.forced_one_token_per_expert_logits(cfg)
+        acts = dataclasses.replace(acts, logits=forced_logits)
     w = synth.make_weights(cfg, seed=0, device=str(dev))
     layer = MoELayer.from_config(cfg, w)
     keep_master = rank == 0 and world == 1 and is_main and not args.no_cpu_baseline
@@ -427,7 +435,8 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4" if a4 else "bf16", "data": "synthetic",
-        "config": {"workload": f"{cfg.name} moe layer, {cfg.w_fmt} weights, {cfg.act_fmt} activations, T={T}",
+        "config": {"workload": f"{cfg.name} moe layer, {cfg.w_fmt} weights, {cfg.act_fmt} activations, T={T}"
+                               + (", routing forced to one token per expert" if args.forced else ""),
                    "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "I_s": cfg.I_s, "T": T, "zipf": cfg.zipf,
                    "seed": 0, "active_experts": active,
                    "l2": "flushed before every step (256 MB write, outside the events)",
@@ -552,6 +561,8 @@ def main():
                     help="run the DeepSeek-V3-shape size / imbalance sweep (one JSON line per point)")
     ap.add_argument("--sweep-ts", default=None, help="comma-separated T values of the sweep (default 1..65536)")
     ap.add_argument("--sweep-steps", type=int, default=10, help="timed steps per sweep point")
+    ap.add_argument("--forced", action="store_true",
+                    help="route every expert exactly one token (T = E / k; the decode microbenchmark shape)")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling variant: this many experts, tokens scaled to keep tokens per expert")
     args = ap.parse_args()
