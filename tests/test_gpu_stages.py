@@ -275,12 +275,14 @@ W4A16_COUNTS = {
     "few": [1, 2, 0, 20, 3, 2, 1, 0, 5, 1],        # <= 4 rows per group on average: 16-token tiles
     "mid": [3, 40, 0, 70, 9, 17, 1, 30],           # 5..48 rows per group: 64-token tiles
     "many": [3, 200, 0, 64, 129, 17],              # > 48 rows per group: 128-token tiles
+    "huge": [300, 0, 129, 250, 64],                # 128-token tiles, groups of two and three blocks
 }
 
 
 @pytest.mark.parametrize("epi,N,K,rows", [(1, 256, 512, "many"), (0, 384, 768, "many"), (1, 192, 320, "many"),
                                           (0, 128, 576, "many"), (1, 256, 1024, "few"), (0, 512, 256, "few"),
-                                          (1, 384, 512, "mid"), (0, 256, 768, "mid")])
+                                          (1, 384, 512, "mid"), (0, 256, 768, "mid"),
+                                          (1, 256, 512, "huge"), (0, 384, 768, "huge")])
 def test_grouped_gemm_nvfp4_weights(epi, N, K, rows):
     """bf16 A x NVFP4 W (codes + E4M3 scales + per-group fp32 scale): K a
     multiple of 256 (weights expanded into tensor memory, fp16 MMA, in each
