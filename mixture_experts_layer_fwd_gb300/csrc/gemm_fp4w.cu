@@ -30,9 +30,11 @@
 //               same features, per k-block), A scales 128 rows x 32 bytes,
 //               B scales likewise
 //   warps 6..9  scale warps (above): sf_full -> shared-memory gather ->
-//               tcgen05.st -> arrive sf_ready (the scale copies are issued
-//               first and complete on their own barrier)
-//   warp 1      TMEM allocation; MMA issuer: waits sf_ready and full, issues up to 8
+//               tcgen05.st -> arrive on the stage's full barrier (the scale
+//               copies are issued first and complete on their own barrier;
+//               the full barrier then covers codes and scales, so the MMA
+//               issuer waits once per stage)
+//   warp 1      TMEM allocation; MMA issuer: waits full, issues up to 8
 //               block-scaled MMAs M=128 N=128 K=64 into one of two
 //               128-column fp32 accumulators, commits the stage free
 //   warps 2..5  epilogue (shared with the other kernels): global scales
@@ -95,8 +97,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
   uint8_t* stages = base;
   uint64_t* full = reinterpret_cast<uint64_t*>(base + S * STAGE_BYTES);
   uint64_t* sf_full = full + S;
-  uint64_t* sf_ready = sf_full + S;
-  uint64_t* empty = sf_ready + S;
+  uint64_t* empty = sf_full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
@@ -113,9 +114,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + 4);  // the producer's arm + one arrival per scale warp
       mbar_init(&sf_full[s], 1);
-      mbar_init(&sf_ready[s], 4);  // one arrival per scale warp
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(&sf_ready[stage], phase, tmo, p.err, abort_flag) ||
-              !mbar_wait_bounded(&full[stage], phase, tmo, p.err, abort_flag)) {
+          // codes landed and the scale warps' tensor-memory stores are done
+          if (!mbar_wait_bounded(&full[stage], phase, tmo, p.err, abort_flag)) {
             ok = false;
             break;
           }
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_ready[stage]);
+        if (lane == 0) mbar_arrive(&full[stage]);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
