@@ -10,8 +10,8 @@ values in tests/golden/.  No function here is "parity unpinned".
 """
 from . import nvfp4
 from .moe import (ExpertWeights, Permutation, expert_mlp, forward, gather_rows,
-                  permute, rel_frobenius, route, silu, unpermute)
+                  permute, rel_frobenius, route, shared_gate, sigmoid, silu, unpermute)
 
 __all__ = ["nvfp4", "ExpertWeights", "Permutation", "expert_mlp", "forward",
-           "gather_rows", "permute", "rel_frobenius", "route", "silu",
-           "unpermute"]
+           "gather_rows", "permute", "rel_frobenius", "route", "shared_gate",
+           "sigmoid", "silu", "unpermute"]

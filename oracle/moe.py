@@ -52,7 +52,7 @@ F32 = np.float32
 # ----------------------------------------------------------------------------
 # route
 # ----------------------------------------------------------------------------
-def route(logits: np.ndarray, k: int):
+def route(logits: np.ndarray, k: int, renorm: bool = True):
     """Top-k routing with renormalised softmax weights.
 
     logits: fp32 [T, E].  Returns idx int32 [T, k] (descending logit, ties to
@@ -60,6 +60,11 @@ def route(logits: np.ndarray, k: int):
         w_j = exp(l_j - l_max) / sum_{i in selected} exp(l_i - l_max),
     which equals the full softmax over E renormalised over the k selected
     experts (the full denominator cancels).
+
+    renorm=False: the variant without renormalisation (the pages allude to
+    router variants without fixing one; reading taken: the same selection,
+    weights = the full softmax over all E logits at the selected experts),
+        w_j = exp(l_j - l_max) / sum_{e < E} exp(l_e - l_max).
     """
     logits = np.asarray(logits, dtype=F32)
     T, E = logits.shape
@@ -71,7 +76,11 @@ def route(logits: np.ndarray, k: int):
     if T == 0:
         return idx, np.zeros((0, k), np.float64)
     z = np.exp(sel - sel[:, :1])
-    w = z / z.sum(axis=1, keepdims=True)
+    if renorm:
+        w = z / z.sum(axis=1, keepdims=True)
+    else:
+        full = np.exp(logits.astype(np.float64) - sel[:, :1]).sum(axis=1, keepdims=True)
+        w = z / full
     return idx, w
 
 
@@ -157,12 +166,30 @@ class ExpertWeights:
     w2: np.ndarray
 
 
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    """1 / (1 + e^-z), evaluated through e^-|z| so that it never overflows."""
+    z = np.asarray(z, dtype=np.float64)
+    e = np.exp(-np.abs(z))
+    return np.where(z >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def shared_gate(x_gate: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """Per-token gate of the shared expert, sigma(x_t . g) ("Hosting Qwen on
+    Blackwell" names new gate terms without fixing them; reading taken: a
+    sigmoid of the token's dot product with one gate vector g [H], applied
+    to the shared expert's output, computed from the bf16 activations)."""
+    return sigmoid(np.asarray(x_gate, np.float64) @ np.asarray(g, np.float64))
+
+
 def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
             get_expert: Callable[[int], ExpertWeights],
             shared: Optional[ExpertWeights] = None,
             tokens: Optional[Sequence[int]] = None,
             h_quant_g: Optional[np.float32] = None,
-            hs_quant_g: Optional[np.float32] = None):
+            hs_quant_g: Optional[np.float32] = None,
+            renorm: bool = True,
+            shared_g: Optional[np.ndarray] = None,
+            x_gate: Optional[np.ndarray] = None):
     """Layer output for the given tokens (all tokens when `tokens` is None).
 
     x_deq   : fp64 [T, H] the activations as the experts see them (bf16 values,
@@ -172,10 +199,13 @@ def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
               tokens use (lets the caller decode weights lazily)
     Returns (out fp64 [len(tokens), H], idx, w, perm) where idx / w / perm
     cover the full T (routing is cheap) and out covers `tokens`.
+    renorm  : False selects the router without renormalisation (see route)
+    shared_g: gate vector [H] of the shared expert (None: ungated, weight 1);
+              x_gate: the activations the gate sees ([T, H]; default x_deq)
     """
     x_deq = np.asarray(x_deq, dtype=np.float64)
     T, H = x_deq.shape
-    idx, w = route(logits, k)
+    idx, w = route(logits, k, renorm)
     perm = permute(idx, E)
     toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     out = np.zeros((len(toks), H), dtype=np.float64)
@@ -194,7 +224,11 @@ def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
             j = int(np.nonzero(perm.row_of[t] == r)[0][0])
             out[pos[int(t)]] += w[t, j] * yr
     if shared is not None:
-        out += expert_mlp(x_deq[toks], shared.w13, shared.w2, hs_quant_g)
+        ys = expert_mlp(x_deq[toks], shared.w13, shared.w2, hs_quant_g)
+        if shared_g is not None:
+            xg = x_deq if x_gate is None else np.asarray(x_gate, np.float64)
+            ys = ys * shared_gate(xg[toks], shared_g)[:, None]
+        out += ys
     return out, idx, w, perm
 
 

@@ -336,3 +336,69 @@ def test_deepseek_h_scale_rarely_saturates():
     h = (lambda g, u: g / (1 + np.exp(-g)) * u)(x @ w13[:I].T, x @ w13[I:].T)
     frac = np.mean(np.abs(h) > 6 * 448 * cfg.g_h)
     assert frac < 1e-4 and np.abs(h).max() > 1.0
+
+
+# ------------------------------------------- router / shared-gate variants ----
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (50, 128, 8), (20, 512, 10), (7, 5, 5)])
+def test_route_without_renorm_is_full_softmax_at_the_picks(T, E, k):
+    """renorm=False: the same experts, weights = the full softmax over E
+    (torch's softmax in fp64, a library routine) taken at the picks."""
+    rng = np.random.default_rng(T * E + k)
+    logits = (rng.standard_normal((T, E)) * 3).astype(F32)
+    idx, w = route(logits, k, renorm=False)
+    idx_r, w_r = route(logits, k)
+    assert np.array_equal(idx, idx_r)
+    p = torch.softmax(torch.from_numpy(logits.astype(np.float64)), dim=1).numpy()
+    np.testing.assert_allclose(w, np.take_along_axis(p, idx, axis=1), rtol=1e-13, atol=0)
+    # the renormalised weights are these weights over their sum; the sum is
+    # the probability mass of the picks (1 when k == E)
+    s = w.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(w / s, w_r, rtol=1e-13)
+    assert np.all(s <= 1 + 1e-12)
+    if k == E:
+        np.testing.assert_allclose(s, 1.0, rtol=1e-13)
+
+
+def test_route_without_renorm_uniform_logits():
+    """Equal logits: every pick weighs exactly 1/E (ties to the lower ids)."""
+    T, E, k = 3, 16, 4
+    idx, w = route(np.zeros((T, E), F32), k, renorm=False)
+    assert np.array_equal(idx, np.tile(np.arange(k, dtype=np.int32), (T, 1)))
+    np.testing.assert_allclose(w, 1.0 / E, rtol=1e-15)
+
+
+def test_shared_gate_zero_vector_halves_the_shared_expert():
+    """g = 0: sigma(0) = 1/2 exactly, so the gated layer is the routed part
+    plus half the shared expert."""
+    rng = np.random.default_rng(11)
+    T, H, E, k, I, I_s = 6, 16, 4, 2, 8, 12
+    experts, shared, x, logits = _tiny_layer(rng, T, H, E, k, I, I_s)
+    get = lambda e: experts[e]
+    full, *_ = forward(x, logits, k, E, get, shared)
+    routed, *_ = forward(x, logits, k, E, get, None)
+    gated, *_ = forward(x, logits, k, E, get, shared, shared_g=np.zeros(H))
+    np.testing.assert_allclose(gated, routed + 0.5 * (full - routed), rtol=1e-13, atol=1e-15)
+
+
+def test_shared_gate_brute_force_scalars():
+    """Gate of every token by a scalar loop (dot product, then 1/(1+e^-z)),
+    and the gated layer against the ungated one row by row."""
+    rng = np.random.default_rng(12)
+    T, H, E, k, I, I_s = 5, 8, 3, 1, 4, 6
+    experts, shared, x, logits = _tiny_layer(rng, T, H, E, k, I, I_s)
+    g = rng.standard_normal(H)
+    get = lambda e: experts[e]
+    full, *_ = forward(x, logits, k, E, get, shared)
+    routed, *_ = forward(x, logits, k, E, get, None)
+    gated, *_ = forward(x, logits, k, E, get, shared, shared_g=g)
+    for t in range(T):
+        z = 0.0
+        for h in range(H):
+            z += x[t, h] * g[h]
+        gate = 1.0 / (1.0 + math.exp(-z))
+        np.testing.assert_allclose(gated[t], routed[t] + gate * (full[t] - routed[t]), rtol=1e-12, atol=1e-14)
+    # a very large positive / negative gate input passes / blocks the shared expert
+    big, *_ = forward(x, logits, k, E, get, shared, shared_g=np.full(H, 1e3), x_gate=np.ones((T, H)))
+    np.testing.assert_allclose(big, full, rtol=1e-12)
+    small, *_ = forward(x, logits, k, E, get, shared, shared_g=np.full(H, -1e3), x_gate=np.ones((T, H)))
+    np.testing.assert_allclose(small, routed, rtol=1e-12, atol=1e-14)
