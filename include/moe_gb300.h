@@ -114,6 +114,14 @@ int moe_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
 int moe_route(const float* logits, int T, int E, int k,
               int32_t* idx, float* w, void* stream);
 
+/* moe_route with a choice of weights.  renorm != 0: as moe_route.  renorm ==
+ * 0: the router without renormalisation (the pages allude to router
+ * variants without fixing one; reading taken): the same experts and order,
+ * w_j = exp(l_j - l_0) / sum_{e<E} exp(l_e - l_0), the full softmax over E
+ * at the picks (so sum_j w_j <= 1).  Same arguments and limits. */
+int moe_route_ex(const float* logits, int T, int E, int k, int renorm,
+                 int32_t* idx, float* w, void* stream);
+
 /* ----------------------------------------------------------------- permute
  * Local dispatch: count tokens per expert, give each routed slot a unique
  * position inside its expert's list, copy the token rows into an
@@ -228,6 +236,25 @@ int moe_combine(const uint16_t* Y, const int32_t* row_of, const float* w,
                 const uint16_t* Ys, int T, int k, int H,
                 uint16_t* out, void* stream);
 
+/* moe_combine with a gated shared expert: the shared row enters as
+ * ys_gate[t] * Ys[t, :] (fp32 multiply-add in the same accumulation order).
+ *   ys_gate : fp32 [T] per-token gate (from moe_shared_gate), or NULL for
+ *             weight 1; requires Ys when given; 4-byte aligned. */
+int moe_combine_gated(const uint16_t* Y, const int32_t* row_of, const float* w,
+                      const uint16_t* Ys, const float* ys_gate, int T, int k, int H,
+                      uint16_t* out, void* stream);
+
+/* Gate of the shared expert ("Hosting Qwen on Blackwell" names new gate
+ * terms without fixing them; reading taken: a sigmoid of the token's dot
+ * product with one gate vector):
+ *   gate[t] = 1 / (1 + exp(-(x_t . g)))   dot in fp32, one warp per token
+ *   x    : bf16 [T, H] activations (before any quantisation)
+ *   g    : bf16 [H]    gate vector
+ *   gate : fp32 [T]
+ * H must be a multiple of 8; x and g 16-byte aligned. */
+int moe_shared_gate(const uint16_t* x, const uint16_t* g, int T, int H,
+                    float* gate, void* stream);
+
 /* ----------------------------------------------------------- whole layer
  * Weight description of one layer.  All pointers are device pointers.
  *   bf16 weights : w13 [E, 2I, H] (rows [0,I) gate, [I,2I) up), w2 [E, H, I],
@@ -239,7 +266,12 @@ int moe_combine(const uint16_t* Y, const int32_t* row_of, const float* w,
  *                  scale over x) before dispatch, and the SwiGLU output h is
  *                  quantised to NVFP4 with the caller's global scales
  *                  *g_h (routed) and *g_hs (shared) before the down GEMM.
- * I_s = 0 means no shared expert. */
+ * I_s = 0 means no shared expert.
+ * Variants (zero-initialised fields keep the default layer):
+ *   no_renorm != 0 : route without renormalisation (moe_route_ex, renorm 0)
+ *   ws_gate        : bf16 [H] gate vector of the shared expert (requires
+ *                    I_s > 0; 16-byte aligned): the shared output is scaled
+ *                    by sigma(x_t . ws_gate) (moe_shared_gate); NULL: weight 1 */
 typedef struct {
   int H, E, k, I, I_s;
   int w_fmt, act_fmt;
@@ -249,6 +281,8 @@ typedef struct {
   const void* ws2;  const uint8_t* ws2_sf;  const float* ws2_g;
   const float* g_h;
   const float* g_hs;
+  int no_renorm;
+  const uint16_t* ws_gate;
 } moe_layer;
 
 /* Workspace bytes moe_forward needs for T tokens (0 on invalid layer). */

@@ -39,6 +39,7 @@ class MoeLayerC(ctypes.Structure):
         ("ws13", c_void_p), ("ws13_sf", c_void_p), ("ws13_g", c_void_p),
         ("ws2", c_void_p), ("ws2_sf", c_void_p), ("ws2_g", c_void_p),
         ("g_h", c_void_p), ("g_hs", c_void_p),
+        ("no_renorm", c_int), ("ws_gate", c_void_p),
     ]
 
 
@@ -51,6 +52,7 @@ SIGNATURES = {
     "moe_sync_status": (c_int, [c_void_p]),
     "moe_selftest_wait_timeout": (c_int, [c_ull, c_void_p]),
     "moe_route": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "moe_route_ex": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_permute_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_permute": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_int, c_void_p, c_int,
                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -65,6 +67,9 @@ SIGNATURES = {
                                  c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                             c_void_p, c_void_p]),
+    "moe_combine_gated": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                  c_void_p, c_void_p]),
+    "moe_shared_gate": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p]),
     "moe_forward_workspace_size": (c_size_t, [ctypes.POINTER(MoeLayerC), c_int]),
     "moe_forward": (c_int, [ctypes.POINTER(MoeLayerC), c_void_p, c_void_p, c_int, c_void_p,
                             c_void_p, c_size_t, c_void_p]),

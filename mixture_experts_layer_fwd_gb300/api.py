@@ -54,8 +54,9 @@ def moe_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
 
 
 def moe_route(logits: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
-              w: Optional[torch.Tensor] = None, stream=None):
-    """logits fp32 [T, E] -> (idx int32 [T, k], w fp32 [T, k])."""
+              w: Optional[torch.Tensor] = None, stream=None, renorm: bool = True):
+    """logits fp32 [T, E] -> (idx int32 [T, k], w fp32 [T, k]); renorm=False
+    takes the full softmax over E at the picks (moe_route_ex)."""
     _dev(logits)
     assert logits.dtype == torch.float32 and logits.dim() == 2
     T, E = logits.shape
@@ -63,7 +64,10 @@ def moe_route(logits: torch.Tensor, k: int, idx: Optional[torch.Tensor] = None,
         idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
     if w is None:
         w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
-    check(load().moe_route(_ptr(logits), T, E, k, _ptr(idx), _ptr(w), _stream(stream)), "moe_route")
+    if renorm:
+        check(load().moe_route(_ptr(logits), T, E, k, _ptr(idx), _ptr(w), _stream(stream)), "moe_route")
+    else:
+        check(load().moe_route_ex(_ptr(logits), T, E, k, 0, _ptr(idx), _ptr(w), _stream(stream)), "moe_route_ex")
     return idx, w
 
 
@@ -171,12 +175,29 @@ def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tenso
 
 
 def moe_combine(Y: torch.Tensor, row_of: torch.Tensor, w: torch.Tensor, Ys: Optional[torch.Tensor],
-                T: int, k: int, H: int, out: Optional[torch.Tensor] = None, stream=None):
+                T: int, k: int, H: int, out: Optional[torch.Tensor] = None, stream=None,
+                ys_gate: Optional[torch.Tensor] = None):
+    """ys_gate: fp32 [T] per-token factor of the shared row (moe_combine_gated)."""
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=Y.device)
-    check(load().moe_combine(_ptr(Y), _ptr(row_of), _ptr(w), _ptr(Ys), T, k, H, _ptr(out), _stream(stream)),
-          "moe_combine")
+    if ys_gate is None:
+        check(load().moe_combine(_ptr(Y), _ptr(row_of), _ptr(w), _ptr(Ys), T, k, H, _ptr(out), _stream(stream)),
+              "moe_combine")
+    else:
+        check(load().moe_combine_gated(_ptr(Y), _ptr(row_of), _ptr(w), _ptr(Ys), _ptr(ys_gate), T, k, H,
+                                       _ptr(out), _stream(stream)), "moe_combine_gated")
     return out
+
+
+def moe_shared_gate(x: torch.Tensor, g: torch.Tensor, gate: Optional[torch.Tensor] = None, stream=None):
+    """x bf16 [T, H], g bf16 [H] -> gate fp32 [T] = sigmoid(x . g)."""
+    _dev(x)
+    assert x.dtype == torch.bfloat16 and g.dtype == torch.bfloat16 and x.dim() == 2
+    T, H = x.shape
+    if gate is None:
+        gate = torch.empty(T, dtype=torch.float32, device=x.device)
+    check(load().moe_shared_gate(_ptr(x), _ptr(g), T, H, _ptr(gate), _stream(stream)), "moe_shared_gate")
+    return gate
 
 
 def moe_forward_workspace_size(layer_c, T: int) -> int:

@@ -18,7 +18,8 @@ constexpr int kCombineBatch = 8;
 
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ w, const uint16_t* __restrict__ Ys,
-                                                      int T, int k, int H, int slices, uint16_t* __restrict__ out) {
+                                                      const float* __restrict__ ys_gate, int T, int k, int H,
+                                                      int slices, uint16_t* __restrict__ out) {
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int t = static_cast<int>(gw / slices);
@@ -61,10 +62,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   if (Ys != nullptr) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(Ys + static_cast<size_t>(t) * H) + c);
     const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+    if (ys_gate != nullptr) {
+      const float gt = __ldg(ys_gate + t);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] += __uint_as_float(q[i] << 16);
-      acc[2 * i + 1] += __uint_as_float(q[i] & 0xFFFF0000u);
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(gt, __uint_as_float(q[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(gt, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(q[i] << 16);
+        acc[2 * i + 1] += __uint_as_float(q[i] & 0xFFFF0000u);
+      }
     }
   }
   uint4 o;
@@ -75,14 +85,46 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c] = o;
 }
 
-int combine_launch(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, int T, int k, int H,
-                   uint16_t* out, cudaStream_t s) {
+// Gate of the shared expert per token, sigma(x_t . g) in fp32, one warp per
+// token ("Hosting Qwen on Blackwell" names new gate terms; reading: a sigmoid
+// of the token's dot product with one gate vector).  HBM-bound: 2 * H bytes
+// of x per token; lane l reads 16-byte chunks l, l+32, ...
+__global__ void __launch_bounds__(256) shared_gate_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
+                                                          int T, int H, float* __restrict__ gate) {
+  const int t = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  float acc = 0.0f;
+  for (int c = lane; c < (H >> 3); c += 32) {
+    const uint4 a = __ldg(xr + c), b = __ldg(gr + c);
+    const uint32_t qa[4] = {a.x, a.y, a.z, a.w}, qb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(qa[i] << 16), __uint_as_float(qb[i] << 16), acc);
+      acc = fmaf(__uint_as_float(qa[i] & 0xFFFF0000u), __uint_as_float(qb[i] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) gate[t] = 1.0f / (1.0f + expf(-acc));
+}
+
+int shared_gate_launch(const uint16_t* x, const uint16_t* g, int T, int H, float* gate, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  shared_gate_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, g, T, H, gate);
+  return check_launch();
+}
+
+int combine_launch(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, const float* ys_gate,
+                   int T, int k, int H, uint16_t* out, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const int slices = (H / 8 + 31) / 32;
   const long long warps = static_cast<long long>(T) * slices;
   const long long blocks = (warps + 7) / 8;
   if (blocks > 0x7FFFFFFFLL) return MOE_ERR_UNSUPPORTED;
-  combine_kernel<<<static_cast<unsigned int>(blocks), 256, 0, s>>>(Y, row_of, w, Ys, T, k, H, slices, out);
+  combine_kernel<<<static_cast<unsigned int>(blocks), 256, 0, s>>>(Y, row_of, w, Ys, ys_gate, T, k, H, slices, out);
   return check_launch();
 }
 
@@ -90,12 +132,28 @@ int combine_launch(const uint16_t* Y, const int32_t* row_of, const float* w, con
 
 using namespace moe;
 
-extern "C" int moe_combine(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, int T, int k,
-                           int H, uint16_t* out, void* stream) {
+extern "C" int moe_combine_gated(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys,
+                                 const float* ys_gate, int T, int k, int H, uint16_t* out, void* stream) {
   if (T < 0 || k < 1 || H < 1) return MOE_ERR_INVALID_ARG;
   if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!Y || !row_of || !w || !out) return MOE_ERR_INVALID_ARG;
-  if (!aligned(Y, 16) || !aligned(out, 16) || (Ys && !aligned(Ys, 16))) return MOE_ERR_INVALID_ARG;
-  return combine_launch(Y, row_of, w, Ys, T, k, H, out, static_cast<cudaStream_t>(stream));
+  if (ys_gate && !Ys) return MOE_ERR_INVALID_ARG;
+  if (!aligned(Y, 16) || !aligned(out, 16) || (Ys && !aligned(Ys, 16)) || (ys_gate && !aligned(ys_gate, 4)))
+    return MOE_ERR_INVALID_ARG;
+  return combine_launch(Y, row_of, w, Ys, ys_gate, T, k, H, out, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_combine(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, int T, int k,
+                           int H, uint16_t* out, void* stream) {
+  return moe_combine_gated(Y, row_of, w, Ys, nullptr, T, k, H, out, stream);
+}
+
+extern "C" int moe_shared_gate(const uint16_t* x, const uint16_t* g, int T, int H, float* gate, void* stream) {
+  if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !g || !gate) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(gate, 4)) return MOE_ERR_INVALID_ARG;
+  return shared_gate_launch(x, g, T, H, gate, static_cast<cudaStream_t>(stream));
 }

@@ -35,6 +35,7 @@ struct FwdBufs {
   uint8_t* hs_sf;
   uint16_t* Y;
   uint16_t* Ys;
+  float* gate;  // shared-expert gate per token (gated layers)
 };
 
 int validate_layer(const moe_layer* L) {
@@ -53,6 +54,7 @@ int validate_layer(const moe_layer* L) {
     if (w4 && (!L->ws13_sf || !L->ws13_g || !L->ws2_sf || !L->ws2_g)) return MOE_ERR_INVALID_ARG;
   }
   if (a4 && (!L->g_h || (L->I_s && !L->g_hs))) return MOE_ERR_INVALID_ARG;
+  if (L->ws_gate && (!L->I_s || !aligned(L->ws_gate, 16))) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -95,6 +97,7 @@ size_t carve(const moe_layer* L, int T, void* ws, size_t cap, FwdBufs* b) {
   }
   b->Y = c.take<uint16_t>(Tk * L->H);
   if (L->I_s) b->Ys = c.take<uint16_t>(static_cast<size_t>(T) * L->H);
+  b->gate = (L->I_s && L->ws_gate) ? c.take<float>(T) : nullptr;
   return c.used;
 }
 
@@ -109,7 +112,8 @@ extern "C" size_t moe_forward_workspace_size(const moe_layer* L, int T) {
   return carve(L, T, nullptr, 0, &b);
 }
 
-extern "C" int moe_route(const float* logits, int T, int E, int k, int32_t* idx, float* w, void* stream);
+extern "C" int moe_route_ex(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
+                            void* stream);
 
 namespace {
 inline int mark(void* const* events, int i, cudaStream_t s) {
@@ -147,7 +151,8 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
   const int Tk = T * k;
 
   MOE_TRY(mark(events, 0, s));
-  MOE_TRY(moe_route(logits, T, E, k, b.idx, b.w, stream));
+  MOE_TRY(moe_route_ex(logits, T, E, k, L->no_renorm ? 0 : 1, b.idx, b.w, stream));
+  if (b.gate) MOE_TRY(shared_gate_launch(x, L->ws_gate, T, H, b.gate, s));
   MOE_TRY(mark(events, 1, s));
   if (a4) MOE_TRY(quant_launch(x, 1, T, H, nullptr, b.xq, b.xsf, b.gx, b.qws, quant_ws_bytes(1), s));
   MOE_TRY(mark(events, 2, s));
@@ -184,7 +189,7 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
                               s));
 
   MOE_TRY(mark(events, 5, s));
-  MOE_TRY(combine_launch(b.Y, b.row_of, b.w, b.Ys, T, k, H, out, s));
+  MOE_TRY(combine_launch(b.Y, b.row_of, b.w, b.Ys, b.gate, T, k, H, out, s));
   return mark(events, 6, s);
 }
 

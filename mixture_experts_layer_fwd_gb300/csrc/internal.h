@@ -15,8 +15,9 @@ size_t quant_ws_bytes(int groups);
 int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float* g_in, uint8_t* codes, uint8_t* sf,
                  float* g_out, void* ws, size_t ws_bytes, cudaStream_t s);
 
-int combine_launch(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, int T, int k, int H,
-                   uint16_t* out, cudaStream_t s);
+int combine_launch(const uint16_t* Y, const int32_t* row_of, const float* w, const uint16_t* Ys, const float* ys_gate,
+                   int T, int k, int H, uint16_t* out, cudaStream_t s);
+int shared_gate_launch(const uint16_t* x, const uint16_t* g, int T, int H, float* gate, cudaStream_t s);
 
 // One problem set of the grouped GEMM: all routed groups (rows given by
 // device offsets), or the shared expert as a single group over all tokens.

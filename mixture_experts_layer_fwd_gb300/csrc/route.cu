@@ -11,6 +11,9 @@
 // in descending order; lane j keeps the j-th pick.  The weights are the
 // softmax over the k picked logits, which equals the full softmax over E
 // renormalised over the picks because the full denominator cancels.
+// Without renormalisation (a router variant the pages allude to) the weights
+// are the full softmax over all E logits at the picks: the warp also sums
+// exp(l - l_max) over its lanes' logits.
 #include <cfloat>
 
 #include "common.cuh"
@@ -19,7 +22,7 @@ namespace moe {
 
 template <int EPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                    int32_t* __restrict__ idx, float* __restrict__ w) {
+                                                    int renorm, int32_t* __restrict__ idx, float* __restrict__ w) {
   const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -67,6 +70,12 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
   }
   const float z = (lane < k) ? expf(my_val - top) : 0.0f;
   float sum = z;
+  if (!renorm) {
+    sum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if (lane + 32 * j < E) sum += expf(v[j] - top);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
   if (lane < k) {
@@ -80,7 +89,8 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 
 using namespace moe;
 
-extern "C" int moe_route(const float* logits, int T, int E, int k, int32_t* idx, float* w, void* stream) {
+extern "C" int moe_route_ex(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
+                            void* stream) {
   if (T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > E || k > 32 || E > 1024) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
@@ -91,16 +101,20 @@ extern "C" int moe_route(const float* logits, int T, int E, int k, int32_t* idx,
   const int blocks = (T + 7) / 8;
   const int epl = (E + 31) / 32;
   if (epl <= 1)
-    route_kernel<1><<<blocks, threads, 0, s>>>(logits, T, E, k, idx, w);
+    route_kernel<1><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm ? 1 : 0, idx, w);
   else if (epl <= 2)
-    route_kernel<2><<<blocks, threads, 0, s>>>(logits, T, E, k, idx, w);
+    route_kernel<2><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm ? 1 : 0, idx, w);
   else if (epl <= 4)
-    route_kernel<4><<<blocks, threads, 0, s>>>(logits, T, E, k, idx, w);
+    route_kernel<4><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm ? 1 : 0, idx, w);
   else if (epl <= 8)
-    route_kernel<8><<<blocks, threads, 0, s>>>(logits, T, E, k, idx, w);
+    route_kernel<8><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm ? 1 : 0, idx, w);
   else if (epl <= 16)
-    route_kernel<16><<<blocks, threads, 0, s>>>(logits, T, E, k, idx, w);
+    route_kernel<16><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm ? 1 : 0, idx, w);
   else
-    route_kernel<32><<<blocks, threads, 0, s>>>(logits, T, E, k, idx, w);
+    route_kernel<32><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm ? 1 : 0, idx, w);
   return check_launch();
+}
+
+extern "C" int moe_route(const float* logits, int T, int E, int k, int32_t* idx, float* w, void* stream) {
+  return moe_route_ex(logits, T, E, k, 1, idx, w, stream);
 }

@@ -34,11 +34,14 @@ def quantize_weights(w: torch.Tensor) -> NVFP4Tensor:
 class MoELayer:
     def __init__(self, H: int, E: int, k: int, I: int, I_s: int, w13: torch.Tensor, w2: torch.Tensor,
                  ws13: Optional[torch.Tensor] = None, ws2: Optional[torch.Tensor] = None,
-                 w_fmt: str = "bf16", act_fmt: str = "bf16", g_h: float = 0.0, g_hs: Optional[float] = None):
+                 w_fmt: str = "bf16", act_fmt: str = "bf16", g_h: float = 0.0, g_hs: Optional[float] = None,
+                 renorm: bool = True, shared_gate: Optional[torch.Tensor] = None):
         """w13 bf16 [E, 2I, H], w2 bf16 [E, H, I], ws13 bf16 [2I_s, H], ws2 bf16
         [H, I_s] on one CUDA device.  With w_fmt='nvfp4' they are quantised
         here; act_fmt='nvfp4' also needs the static global scale g_h of the
-        SwiGLU output (g_hs for the shared expert, default g_h)."""
+        SwiGLU output (g_hs for the shared expert, default g_h).
+        renorm=False routes without renormalisation; shared_gate (bf16 [H])
+        scales the shared expert by sigmoid(x . shared_gate)."""
         self.H, self.E, self.k, self.I, self.I_s = H, E, k, I, I_s
         self.w_fmt, self.act_fmt = w_fmt, act_fmt
         self.device = w13.device
@@ -70,6 +73,13 @@ class MoELayer:
             self.g_h = torch.tensor([g_h], dtype=torch.float32, device=self.device)
             self.g_hs = torch.tensor([g_h if g_hs is None else g_hs], dtype=torch.float32, device=self.device)
             c.g_h, c.g_hs = self.g_h.data_ptr(), self.g_hs.data_ptr()
+        c.no_renorm = 0 if renorm else 1
+        if shared_gate is not None:
+            if not I_s:
+                raise ValueError("a shared-expert gate needs a shared expert (I_s > 0)")
+            self.shared_gate = shared_gate.to(device=self.device, dtype=torch.bfloat16).contiguous()
+            c.ws_gate = self.shared_gate.data_ptr()
+            self._keep.append(self.shared_gate)
         self.c = c
         self._ws = None
 

@@ -63,8 +63,11 @@ class OracleWeights:
         return self.cache["shared"]
 
 
-def oracle_layer(cfg: synth.LayerConfig, acts: synth.Activations, ow: OracleWeights, tokens=None):
-    """Oracle output (fp64) for the given tokens, plus idx / w / perm over all T."""
+def oracle_layer(cfg: synth.LayerConfig, acts: synth.Activations, ow: OracleWeights, tokens=None,
+                 renorm: bool = True, shared_g=None):
+    """Oracle output (fp64) for the given tokens, plus idx / w / perm over all T.
+    renorm / shared_g select the router and shared-gate variants (the gate sees
+    the bf16 activations)."""
     x = to_np_f32(acts.x)
     if cfg.act_fmt == "nvfp4":
         q, s, g = nvfp4.quantize(x)  # one global scale over the whole input
@@ -74,4 +77,6 @@ def oracle_layer(cfg: synth.LayerConfig, acts: synth.Activations, ow: OracleWeig
         x_deq = x.astype(np.float64)
         gh = None
     return oracle.forward(x_deq, acts.logits.numpy(), cfg.k, cfg.E, ow.expert, ow.shared(), tokens=tokens,
-                          h_quant_g=gh, hs_quant_g=gh)
+                          h_quant_g=gh, hs_quant_g=gh, renorm=renorm,
+                          shared_g=None if shared_g is None else to_np_f32(shared_g).astype(np.float64),
+                          x_gate=x.astype(np.float64))

@@ -141,3 +141,25 @@ def test_sweep_points(w_fmt, zipf, T):
     toks = synth.sample_tokens(T, 2, seed=T)
     err, *_ = _run(cfg, T, seed=0, tokens=toks)
     assert err <= _tol(cfg), err
+
+
+@pytest.mark.parametrize("name", ["qwen35-397b", "deepseek-v3"])
+@pytest.mark.parametrize("renorm,gated", [(False, False), (True, True), (False, True)])
+def test_layer_router_and_shared_gate_variants(name, renorm, gated):
+    """The router without renormalisation and the sigmoid-gated shared expert
+    (layer options no_renorm / ws_gate) against the oracle's variants."""
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
+    cfg = SMALL[name]
+    T = 137
+    acts = synth.make_activations(cfg, T, seed=5)
+    w = synth.make_weights(cfg, seed=5, device=DEV)
+    g = (torch.randn(cfg.H, generator=torch.Generator().manual_seed(6)) * 0.05).to(torch.bfloat16)
+    layer = MoELayer(cfg.H, cfg.E, cfg.k, cfg.I, cfg.I_s, w.w13, w.w2, w.ws13, w.ws2, cfg.w_fmt, cfg.act_fmt,
+                     cfg.g_h, renorm=renorm, shared_gate=g.to(DEV) if gated else None)
+    out = layer(acts.x.to(DEV), acts.logits.to(DEV))
+    assert moe_sync_status() == 0
+    got = to_np_f32(out)
+    ref, idx, wts, _ = oracle_layer(cfg, acts, OracleWeights(cfg, w), renorm=renorm, shared_g=g if gated else None)
+    assert oracle.rel_frobenius(got, ref) <= _tol(cfg)
+    if not renorm:
+        assert np.all(wts.sum(axis=1) < 1.0)  # the variant's weights do not sum to one

@@ -215,6 +215,51 @@ def test_combine(T, k, H, shared):
     assert err < 3e-3, err
 
 
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (300, 33, 5), (77, 1024, 32), (500, 512, 10), (64, 4, 4)])
+def test_route_without_renorm(T, E, k):
+    """moe_route_ex(renorm=0): the same experts as the oracle (bit-exact), and
+    weights = the full softmax over E at the picks within 1e-6."""
+    g = torch.Generator().manual_seed(T + E + k)
+    logits = torch.randn(T, E, generator=g) * 2
+    idx, w = api().moe_route(logits.to(DEV), k, renorm=False)
+    _sync()
+    ridx, rw = oracle.route(logits.numpy(), k, renorm=False)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("T,H", [(1, 8), (300, 4096), (77, 7168)])
+def test_shared_gate(T, H):
+    """moe_shared_gate: sigmoid(x . g) per token in fp32 against the oracle."""
+    g0 = torch.Generator().manual_seed(T + H)
+    x = torch.randn(T, H, generator=g0).to(torch.bfloat16)
+    gv = (torch.randn(H, generator=g0) * 0.03).to(torch.bfloat16)
+    gate = api().moe_shared_gate(x.to(DEV), gv.to(DEV))
+    _sync()
+    ref = oracle.shared_gate(x.double().numpy(), gv.double().numpy())
+    np.testing.assert_allclose(gate.cpu().numpy(), ref, rtol=0, atol=2e-6)
+
+
+def test_combine_gated():
+    """moe_combine_gated: the shared row scaled by a per-token gate."""
+    T, k, H = 200, 8, 1024
+    E = 4 * k
+    idx = _zipf_idx(T, E, k, 1.1, seed=3)
+    p = oracle.permute(idx, E)
+    g = torch.Generator().manual_seed(13)
+    _, w = oracle.route(torch.randn(T, E, generator=g).numpy(), k)
+    Y = torch.randn(T * k, H, generator=g).to(torch.bfloat16)
+    Ys = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    gate = torch.rand(T, generator=g)
+    wt = torch.from_numpy(w.astype(np.float32))
+    out = api().moe_combine(Y.to(DEV), torch.from_numpy(p.row_of).to(DEV), wt.to(DEV), Ys.to(DEV), T, k, H,
+                            ys_gate=gate.to(DEV))
+    _sync()
+    ref = np.einsum("tj,tjh->th", wt.double().numpy(), Y.double().numpy()[p.row_of])
+    ref += gate.double().numpy()[:, None] * Ys.double().numpy()
+    assert oracle.rel_frobenius(out.float().cpu().numpy(), ref) < 3e-3
+
+
 # ---------------------------------------------------------- grouped GEMM ----
 def _ragged_offsets(counts):
     return torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32)
