@@ -387,13 +387,25 @@ def run_gpu(args):
     if moe_sync_status() != 0:
         raise RuntimeError("device status not clean after warm-up")
 
+    graph = api.ForwardGraph(layer.c, x, logits, out, ws) if args.graph else None
+    if graph is not None:
+        for _ in range(3):
+            graph.launch()
+        torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     barrier(world)
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
-        api.moe_forward_profiled(layer.c, x, logits, out, ws, evsets[i])
+        if graph is None:
+            api.moe_forward_profiled(layer.c, x, logits, out, ws, evsets[i])
+        else:
+            # one graph launch per step: the step's first and last events
+            # bracket it (stage times come from the profiled warm-up below)
+            evsets[i][0].record()
+            graph.launch()
+            evsets[i][6].record()
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
@@ -401,6 +413,12 @@ def run_gpu(args):
         raise RuntimeError("device status not clean after the timed steps")
 
     step_ms = [evs[0].elapsed_time(evs[6]) for evs in evsets]
+    if graph is not None:
+        # per-stage times of the same forward, launched stage by stage
+        for i in range(args.steps):
+            flush.zero_()
+            api.moe_forward_profiled(layer.c, x, logits, out, ws, evsets[i])
+        torch.cuda.synchronize()
     stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(6)] for evs in evsets])
     value, total_s = job_rate(T * args.steps, float(sum(step_ms)) / 1e3, world, dev)
     total_ms = total_s * 1e3
@@ -440,7 +458,7 @@ def run_gpu(args):
                    "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "I_s": cfg.I_s, "T": T, "zipf": cfg.zipf,
                    "seed": 0, "active_experts": active,
                    "l2": "flushed before every step (256 MB write, outside the events)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "cuda_graph": bool(args.graph)},
         "roofline": roof,
         "stage_ms": {n: round(float(np.mean(stage_ms[:, i])), 4) for i, n in
                      enumerate(["route", "quant", "permute", "gemm_gate_up", "gemm_down", "combine"])},
@@ -561,6 +579,8 @@ def main():
                     help="run the DeepSeek-V3-shape size / imbalance sweep (one JSON line per point)")
     ap.add_argument("--sweep-ts", default=None, help="comma-separated T values of the sweep (default 1..65536)")
     ap.add_argument("--sweep-steps", type=int, default=10, help="timed steps per sweep point")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the forward replayed as one CUDA graph (moe_forward_graph_create)")
     ap.add_argument("--forced", action="store_true",
                     help="route every expert exactly one token (T = E / k; the decode microbenchmark shape)")
     ap.add_argument("--experts", type=int, default=None,

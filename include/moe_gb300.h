@@ -321,6 +321,21 @@ int moe_forward_host(const moe_layer* L, const uint16_t* x_host, const float* lo
                      uint16_t* x_dev, float* logits_dev, uint16_t* out_dev,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* moe_forward as a CUDA graph, for launch-bound sizes (decode, small
+ * layers): the layer's kernels are captured once on fixed buffers and
+ * replayed with one launch.  moe_forward_graph_create runs moe_forward once
+ * on `stream` (which sets up the kernels' launch attributes and writes
+ * `out`), then captures it on a stream of its own and returns the
+ * instantiated graph in *graph.  moe_graph_launch replays it on `stream`:
+ * the same layer, T, and buffers (x, logits, out, ws), whose contents may
+ * change between replays.  moe_graph_destroy frees it.  The layer
+ * description and its weights must outlive the graph. */
+int moe_forward_graph_create(const moe_layer* L, const uint16_t* x, const float* logits, int T,
+                             uint16_t* out, void* ws, size_t ws_bytes, void* stream,
+                             void** graph);
+int moe_graph_launch(void* graph, void* stream);
+int moe_graph_destroy(void* graph);
+
 #ifdef __cplusplus
 }
 #endif

@@ -243,3 +243,34 @@ __all__ = ["MOE_FMT_BF16", "MOE_FMT_NVFP4", "MOE_EPI_STORE_BF16", "MOE_EPI_SWIGL
            "moe_selftest_wait_timeout", "moe_route", "moe_permute", "moe_quant_nvfp4",
            "moe_grouped_gemm", "moe_combine", "moe_forward_workspace_size", "moe_forward",
            "moe_forward_profiled", "moe_forward_host"]
+
+
+class ForwardGraph:
+    """moe_forward captured as a CUDA graph on fixed buffers
+    (moe_forward_graph_create): launch() replays the layer with one launch;
+    the contents of x / logits may change between replays, the buffers may
+    not.  Creating it runs the forward once."""
+
+    def __init__(self, layer_c, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                 stream=None):
+        import ctypes
+        self._keep = (layer_c, x, logits, out, ws)
+        h = ctypes.c_void_p()
+        check(load().moe_forward_graph_create(ctypes.byref(layer_c), _ptr(x), _ptr(logits), x.shape[0], _ptr(out),
+                                              _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(h)),
+              "moe_forward_graph_create")
+        self._h = h
+
+    def launch(self, stream=None) -> None:
+        check(load().moe_graph_launch(self._h, _stream(stream)), "moe_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().moe_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -218,3 +218,61 @@ extern "C" int moe_forward_host(const moe_layer* L, const uint16_t* x_host, cons
   }
   return moe_sync_status(stream);
 }
+
+extern "C" int moe_forward_graph_create(const moe_layer* L, const uint16_t* x, const float* logits, int T,
+                                        uint16_t* out, void* ws, size_t ws_bytes, void* stream, void** graph) {
+  if (!graph) return MOE_ERR_INVALID_ARG;
+  *graph = nullptr;
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  // one ordinary run: argument checks, first-launch attribute setup
+  MOE_TRY(moe_forward(L, x, logits, T, out, ws, ws_bytes, stream));
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  cudaStream_t cs = nullptr;
+  e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  cudaGraph_t g = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int st = MOE_OK;
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    st = moe_forward(L, x, logits, T, out, ws, ws_bytes, cs);
+    e = cudaStreamEndCapture(cs, &g);  // ends the capture whatever moe_forward returned
+    if (st == MOE_OK && e == cudaSuccess) e = cudaGraphInstantiate(&exec, g, 0);
+  }
+  if (g) cudaGraphDestroy(g);
+  cudaStreamDestroy(cs);
+  if (st != MOE_OK) return st;
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  *graph = exec;
+  return MOE_OK;
+}
+
+extern "C" int moe_graph_launch(void* graph, void* stream) {
+  if (!graph) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(graph), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+extern "C" int moe_graph_destroy(void* graph) {
+  if (!graph) return MOE_OK;
+  cudaError_t e = cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(graph));
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}

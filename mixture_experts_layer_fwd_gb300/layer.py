@@ -109,3 +109,10 @@ class MoELayer:
         return api.moe_forward(self.c, x, logits, out, self.workspace(T), stream)
 
     __call__ = forward
+
+    def capture(self, x: torch.Tensor, logits: torch.Tensor, out: Optional[torch.Tensor] = None,
+                stream=None) -> "api.ForwardGraph":
+        """The forward on these buffers as a CUDA graph (one launch per replay)."""
+        if out is None:
+            out = torch.empty(x.shape[0], self.H, dtype=torch.bfloat16, device=self.device)
+        return api.ForwardGraph(self.c, x, logits, out, self.workspace(x.shape[0]), stream)

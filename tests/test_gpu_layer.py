@@ -163,3 +163,28 @@ def test_layer_router_and_shared_gate_variants(name, renorm, gated):
     assert oracle.rel_frobenius(got, ref) <= _tol(cfg)
     if not renorm:
         assert np.all(wts.sum(axis=1) < 1.0)  # the variant's weights do not sum to one
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek-v3"])
+def test_forward_graph_replays_the_layer(name):
+    """moe_forward captured as a CUDA graph: a replay equals the direct
+    forward bit for bit (the kernels are deterministic), also after the
+    inputs' contents change in place."""
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
+    cfg = synth.TINY if name == "tiny" else SMALL[name]
+    T = 64
+    w = synth.make_weights(cfg, seed=3, device=DEV)
+    layer = MoELayer.from_config(cfg, w)
+    a0 = synth.make_activations(cfg, T, seed=3)
+    a1 = synth.make_activations(cfg, T, seed=4)
+    x, lg = a0.x.to(DEV).contiguous(), a0.logits.to(DEV).contiguous()
+    gout = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=DEV)
+    graph = layer.capture(x, lg, gout)
+    for a in (a0, a1):
+        x.copy_(a.x.to(DEV))
+        lg.copy_(a.logits.to(DEV))
+        graph.launch()
+        direct = layer(a.x.to(DEV), a.logits.to(DEV))
+        assert moe_sync_status() == 0
+        assert torch.equal(gout, direct)
+    graph.close()
