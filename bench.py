@@ -17,9 +17,9 @@ grouped-GEMM kernel time live.
 Prints one JSON line.  --impl reference times the fp64 CPU oracle on the
 same workload (bounded token samples per step) instead.
 
-Multi-GPU: the layer forward does not shard in this build (one GPU per
-process); under torchrun each rank runs an independent replica on its own
-GPU and the job value is the sum of tokens over the max per-rank time.
+Multi-GPU: the layer forward runs whole on each GPU (one GPU per process);
+under torchrun each rank runs an independent replica on its own GPU and the
+job value is the sum of tokens over the max per-rank time.
 """
 from __future__ import annotations
 

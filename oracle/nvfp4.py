@@ -18,8 +18,8 @@ section on Blackwell support: abs-max over 16 elements for NVFP4):
 
 Decoded value = e2m1(q) * e4m3(s) * g.
 
-The pages leave the rounding recipe open.  The reading taken (and stated in
-the design doc) is, in IEEE fp32 arithmetic with round-to-nearest-even:
+The pages leave the rounding recipe open.  The reading taken is, in IEEE
+fp32 arithmetic with round-to-nearest-even:
 
     amax = max |x|                  over the tensor (or one group of it)
     g    = amax / 2688              (2688 = 6 * 448); g = 1 when amax == 0
