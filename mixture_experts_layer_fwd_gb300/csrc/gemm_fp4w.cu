@@ -23,7 +23,8 @@
 // operand would cost the stage more issue time than its MMAs).
 //
 // Roles (one CTA per SM):
-//   warp 0      TMA producer, four copies per stage, each with the stage's
+//   warps 0, 10 TMA producers (warp 0 the codes, warp 10 the scales), four
+//               copies per stage, each with the stage's
 //               two 256-element k-blocks as the outer box dimension:
 //               A codes 128 rows x 2 x 128 bytes (128-byte swizzle), B codes
 //               likewise (SwiGLU: 64 gate rows then the 64 up rows of the
@@ -71,7 +72,8 @@ constexpr int STAGES = 3;
 // separate barriers so that the scale warps start before the codes land
 constexpr uint32_t TX_CODES = OFF_SFA;
 constexpr uint32_t TX_SF = STAGE_BYTES - OFF_SFA;
-constexpr int NUM_WARPS = 10;
+constexpr int SF_PROD_WARP = 10;           // producer of the scale copies
+constexpr int NUM_WARPS = 11;
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int TMEM_COLS = 512;
 constexpr int ACC_COLS = 2 * BN;
@@ -138,14 +140,21 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
   const int total = s_prefix[GT];
   const unsigned long long tmo = p.timeout_ns;
 
-  if (warp == 0) {
-    // ===================================================== TMA producer
+  if (warp == 0 || warp == SF_PROD_WARP) {
+    // ===================================================== TMA producers
+    // warp 0 issues the code copies, SF_PROD_WARP the scale copies (a thread's
+    // barrier operations queue behind its own outstanding copies, so two
+    // issuing threads shorten each stage's issue)
     if (lane == 0) {
+      const bool codes = warp == 0;
       for (int pb = 0; pb < (p.shared_rows >= 0 ? 2 : 1); ++pb) {
-        tma_prefetch_desc(&p.tma_a[pb]);
-        tma_prefetch_desc(&p.tma_w[pb]);
-        tma_prefetch_desc(&p.tma_asf[pb]);
-        tma_prefetch_desc(&p.tma_wsf[pb]);
+        if (codes) {
+          tma_prefetch_desc(&p.tma_a[pb]);
+          tma_prefetch_desc(&p.tma_w[pb]);
+        } else {
+          tma_prefetch_desc(&p.tma_asf[pb]);
+          tma_prefetch_desc(&p.tma_wsf[pb]);
+        }
       }
       int stage = 0;
       uint32_t phase = 0;
@@ -169,18 +178,21 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
           }
           uint8_t* sb = stages + stage * STAGE_BYTES;
           const int kblk = kb * KBLK;
-          mbar_arrive_expect_tx(&sf_full[stage], TX_SF);
-          tma_load_2d(&p.tma_asf[ti.pb], &sf_full[stage], sb + OFF_SFA, kb * 32, a_y);
-          if (SWIGLU)
-            tma_load_3d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, kb * 32, f0, 2 * ti.g);
-          else
-            tma_load_2d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, kb * 32, w_y);
-          mbar_arrive_expect_tx(&full[stage], TX_CODES);
-          tma_load_3d(&p.tma_a[ti.pb], &full[stage], sb, 0, a_y, kblk);
-          if (SWIGLU)
-            tma_load_4d(&p.tma_w[ti.pb], &full[stage], sb + OFF_B, 0, f0, 2 * ti.g, kblk);
-          else
-            tma_load_3d(&p.tma_w[ti.pb], &full[stage], sb + OFF_B, 0, w_y, kblk);
+          if (!codes) {
+            mbar_arrive_expect_tx(&sf_full[stage], TX_SF);
+            tma_load_2d(&p.tma_asf[ti.pb], &sf_full[stage], sb + OFF_SFA, kb * 32, a_y);
+            if (SWIGLU)
+              tma_load_3d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, kb * 32, f0, 2 * ti.g);
+            else
+              tma_load_2d(&p.tma_wsf[ti.pb], &sf_full[stage], sb + OFF_SFB, kb * 32, w_y);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], TX_CODES);
+            tma_load_3d(&p.tma_a[ti.pb], &full[stage], sb, 0, a_y, kblk);
+            if (SWIGLU)
+              tma_load_4d(&p.tma_w[ti.pb], &full[stage], sb + OFF_B, 0, f0, 2 * ti.g, kblk);
+            else
+              tma_load_3d(&p.tma_w[ti.pb], &full[stage], sb + OFF_B, 0, w_y, kblk);
+          }
           issued[stage] += 1;
           if (++stage == S) {
             stage = 0;
@@ -191,10 +203,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
       if (!ok) {
         // let copies already issued land before the block can exit
         for (int s = 0; s < S; ++s)
-          if (issued[s]) {
-            mbar_wait_bounded(&full[s], (issued[s] - 1u) & 1u, 1000000000ull, p.err, nullptr);
-            mbar_wait_bounded(&sf_full[s], (issued[s] - 1u) & 1u, 1000000000ull, p.err, nullptr);
-          }
+          if (issued[s])
+            mbar_wait_bounded(codes ? &full[s] : &sf_full[s], (issued[s] - 1u) & 1u, 1000000000ull, p.err, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -248,7 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4w_kernel(const __
         mbar_wait_bounded(drain, 0, 1000000000ull, p.err, nullptr);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // ===================================================== scale warps
     const int q = warp & 3;  // lane quadrant this warp writes
     int stage = 0;
