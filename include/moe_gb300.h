@@ -41,6 +41,10 @@
  *    Each is bounded in time (moe_set_wait_timeout_ns, default 1 s); a wait
  *    that runs out records MOE_ERR_TIMEOUT in a device error word and the
  *    kernel returns.  moe_sync_status() reports (and clears) it.
+ *  - The first call on each device that launches a permutation or a grouped
+ *    GEMM looks up the device error word (cudaGetSymbolAddress) and sets
+ *    kernel attributes; make such a call once before capturing any of them
+ *    into a CUDA graph yourself (moe_forward_graph_create does it for you).
  *  - Inputs are assumed finite; NaN / Inf inputs give unspecified results.
  *  - T = 0 (no tokens) is a valid no-op returning MOE_OK.
  */
@@ -88,8 +92,10 @@ const char* moe_last_cuda_error(void);
 int moe_set_wait_timeout_ns(unsigned long long ns);
 
 /* Synchronises `stream`, then returns MOE_ERR_TIMEOUT if any kernel of this
- * library recorded a wait time-out since the last call (clearing the record),
- * MOE_ERR_CUDA on a CUDA error, else MOE_OK. */
+ * library recorded a wait time-out since the last call, else
+ * MOE_ERR_INVALID_ARG if a permutation met an expert id outside [0, E)
+ * (clearing the record either way), MOE_ERR_CUDA on a CUDA error, else
+ * MOE_OK. */
 int moe_sync_status(void* stream);
 
 /* Test hook for the time-out path: launches one block whose thread waits on
@@ -131,6 +137,10 @@ int moe_route_ex(const float* logits, int T, int E, int k, int renorm,
  * counters accumulated in global memory).
  * The order is deterministic and stable: inside expert e's segment, rows are
  * in ascending token id.  Segments are unpadded.
+ * Ids in idx are read on the device, so they are checked there: a slot whose
+ * id lies outside [0, E) is left out (not counted, row_of = -1, offsets[E]
+ * short by one per such slot, permuted rows past offsets[E] unspecified) and
+ * the next moe_sync_status() returns MOE_ERR_INVALID_ARG.
  *
  *   idx      : int32 [T, k]   expert of each slot (0 <= idx < E, distinct per token)
  *   x_rows   : [T, row_bytes] token rows (bf16 row: 2H bytes; NVFP4 row: H/2
@@ -215,6 +225,9 @@ int moe_quant_nvfp4(const uint16_t* x, int groups, int rows, int cols,
  * fp32 accumulators in tensor memory.
  * Requirements: K % 64 == 0, N % 32 == 0, G <= 1024, M_total < 2^31,
  * offsets non-decreasing with offsets[G] <= M_total; A and W 16-byte aligned.
+ * Offsets are read on the device: each is clamped to [0, M_total] and a
+ * group whose end lies before its start is empty, so offsets that break the
+ * contract give unspecified values but no access outside A, W or C.
  */
 int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue,
                      int G, const int32_t* offsets, int M_total, int N, int K,
@@ -228,6 +241,8 @@ int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue,
  * accumulation in registers using the token positions from dispatch):
  *   out[t, :] = bf16( sum_{j<k} w[t,j] * Y[row_of[t,j], :]  (+ Ys[t, :]) )
  * accumulated in fp32 in the order j = 0..k-1, then the shared expert row.
+ * An entry of row_of outside [0, T*k) (the -1 of a left-out slot) adds
+ * nothing.
  *   Y  : bf16 [T*k, H]   expert outputs in permuted order
  *   Ys : bf16 [T, H]     shared expert output, or NULL
  *   out: bf16 [T, H]
@@ -328,8 +343,11 @@ int moe_forward_host(const moe_layer* L, const uint16_t* x_host, const float* lo
  * `out`), then captures it on a stream of its own and returns the
  * instantiated graph in *graph.  moe_graph_launch replays it on `stream`:
  * the same layer, T, and buffers (x, logits, out, ws), whose contents may
- * change between replays.  moe_graph_destroy frees it.  The layer
- * description and its weights must outlive the graph. */
+ * change between replays.  moe_graph_destroy frees it.  The moe_layer
+ * struct is read only while the graph is created; the weights, scales and
+ * buffers it and the call point to must outlive the graph.  The wait limit
+ * (moe_set_wait_timeout_ns) in force at creation is the one the replays
+ * use. */
 int moe_forward_graph_create(const moe_layer* L, const uint16_t* x, const float* logits, int T,
                              uint16_t* out, void* ws, size_t ws_bytes, void* stream,
                              void** graph);

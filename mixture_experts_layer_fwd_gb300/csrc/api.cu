@@ -12,7 +12,8 @@ namespace moe {
 static char g_last_err[256] = "no error";
 static unsigned long long g_timeout_ns = 1000000000ull;
 
-// One error word per device, set by bounded device waits that run out.
+// One error word per device: bits set by bounded device waits that run out
+// and by the permutation when it meets an expert id outside [0, E).
 __device__ unsigned int g_err_word;
 
 void set_cuda_error(cudaError_t e) {
@@ -198,7 +199,7 @@ int moe_sync_status(void* stream) {
       set_cuda_error(e);
       return MOE_ERR_CUDA;
     }
-    return MOE_ERR_TIMEOUT;
+    return (v & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_INVALID_ARG;
   }
   return MOE_OK;
 }

@@ -9,7 +9,9 @@
 // shared expert, it accumulates w[t,j] * Y[row_of[t,j]] before one round to
 // bf16.  HBM-bound: reads k + 1 rows, writes one.  The slice split keeps
 // enough warps in flight at decode sizes (a few hundred tokens), and the k
-// rows' loads are issued in batches of 8 before their FMAs.
+// rows' loads are issued in batches of 8 before their FMAs.  A row index
+// outside [0, T*k) (the -1 the permutation leaves for a slot whose expert id
+// was out of range) contributes nothing.
 #include "internal.h"
 
 namespace moe {
@@ -26,6 +28,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   if (t >= T) return;
   const int c = static_cast<int>(gw - static_cast<long long>(t) * slices) * 32 + lane;  // 16-byte chunk
   const bool valid = c < (H >> 3);
+  const long long S = static_cast<long long>(T) * k;  // rows of Y
   // lane j < k holds the j-th row / weight; broadcast by shuffles
   int my_row = 0;
   float my_w = 0.0f;
@@ -44,7 +47,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
       const int j = min(j0 + u, k - 1);
       const int r = __shfl_sync(0xFFFFFFFFu, my_row, j);
       wj[u] = __shfl_sync(0xFFFFFFFFu, my_w, j);
-      v[u] = (valid && j0 + u < k) ? __ldg(reinterpret_cast<const uint4*>(Y + static_cast<size_t>(r) * H) + c)
+      v[u] = (valid && j0 + u < k && r >= 0 && r < S) ? __ldg(reinterpret_cast<const uint4*>(Y + static_cast<size_t>(r) * H) + c)
                                    : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll

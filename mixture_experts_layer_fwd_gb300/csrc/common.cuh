@@ -118,8 +118,11 @@ DEVINL bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_
   return ok != 0;
 }
 
-// Error word values (device side); the host maps them to MOE_ERR_TIMEOUT.
+// Error word bits (device side).  The host maps kErrTimeout to
+// MOE_ERR_TIMEOUT and kErrBadIndex (an expert id outside [0, E) met by the
+// permutation, which then leaves that slot out) to MOE_ERR_INVALID_ARG.
 constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrBadIndex = 2u;
 
 // Bounded wait on an mbarrier phase.  Gives up after `timeout_ns` of wall
 // time (or as soon as *abort is set by another role of the block), records

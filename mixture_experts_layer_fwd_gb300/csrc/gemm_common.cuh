@@ -75,18 +75,22 @@ DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT
 
 // Loads the group offsets and builds the per-group tile prefix in shared
 // memory.  Called by every thread of the block (contains barriers).
+// Offsets are clamped to [0, rows of A] and a group whose end lies before its
+// start gets no tiles, so offsets that break the documented contract (non-
+// decreasing, offsets[G] <= M_total) cannot send a tile outside A or C; the
+// tile decoders only ever land on groups with at least one tile.
 template <int THREADS, int NUM_WARPS, int TM = BM>
 DEVINL void build_schedule(const Params& p, int* s_off, int* s_prefix, int* warp_sums) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
   const int GT = G + (p.shared_rows >= 0 ? 1 : 0);
-  for (int i = threadIdx.x; i <= G; i += THREADS) s_off[i] = p.offsets[i];
+  for (int i = threadIdx.x; i <= G; i += THREADS) s_off[i] = min(max(p.offsets[i], 0), p.prob[0].a_rows);
   __syncthreads();
   const int per = (GT + THREADS - 1) / THREADS;
   const int g0 = threadIdx.x * per;
   int local = 0;
   for (int g = g0; g < min(GT, g0 + per); ++g) {
-    const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
+    const int rows = (g < G) ? max(s_off[g + 1] - s_off[g], 0) : p.shared_rows;
     local += ((rows + TM - 1) / TM) * p.prob[g < G ? 0 : 1].n_tiles;
   }
   int incl = local;
@@ -110,7 +114,7 @@ DEVINL void build_schedule(const Params& p, int* s_off, int* s_prefix, int* warp
   int run = incl - local + (warp ? warp_sums[warp - 1] : 0);
   for (int g = g0; g < min(GT, g0 + per); ++g) {
     s_prefix[g] = run;
-    const int rows = (g < G) ? (s_off[g + 1] - s_off[g]) : p.shared_rows;
+    const int rows = (g < G) ? max(s_off[g + 1] - s_off[g], 0) : p.shared_rows;
     run += ((rows + TM - 1) / TM) * p.prob[g < G ? 0 : 1].n_tiles;
   }
   if (threadIdx.x == 0) s_prefix[GT] = warp_sums[NUM_WARPS - 1];

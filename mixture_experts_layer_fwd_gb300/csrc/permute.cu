@@ -20,6 +20,9 @@
 //                counter per expert carries the running position
 //   4. gather  : one warp per permuted row copies the token row (16-byte
 //                vectors) and its scale bytes
+// An expert id outside [0, E) is a caller error: its slot is left out (not
+// counted, row_of = -1, no permuted row), the device error word records
+// kErrBadIndex, and no kernel touches memory outside its buffers.
 #include "internal.h"
 
 namespace moe {
@@ -28,14 +31,20 @@ constexpr int kPermChunk = 1024;   // slots per chunk
 constexpr int kMaxExperts = 4096;
 
 __global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __restrict__ idx, int S, int E,
-                                                            int32_t* __restrict__ hist) {
+                                                            int32_t* __restrict__ hist, unsigned int* err) {
   extern __shared__ int32_t sh[];
   const int c = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
   const int lo = c * kPermChunk;
   const int hi = min(S, lo + kPermChunk);
-  for (int s = lo + threadIdx.x; s < hi; s += blockDim.x) atomicAdd(&sh[__ldg(idx + s)], 1);
+  for (int s = lo + threadIdx.x; s < hi; s += blockDim.x) {
+    const int e = __ldg(idx + s);
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+      atomicAdd(&sh[e], 1);
+    else if (err != nullptr)
+      atomicOr(err, kErrBadIndex);
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(c) * E + e] = sh[e];
 }
@@ -128,10 +137,10 @@ __global__ void __launch_bounds__(32) permute_assign_kernel(const int32_t* __res
   for (int j = 0; j < J; ++j) {
     const int s = lo + 32 * j + lane;
     if (lo + 32 * j >= hi) break;
-    const bool act = s < hi;
+    const int e = ev[j];
+    const bool act = s < hi && static_cast<unsigned>(e) < static_cast<unsigned>(E);
     const unsigned mask = __ballot_sync(0xFFFFFFFFu, act);
     if (act) {
-      const int e = ev[j];
       const unsigned peers = __match_any_sync(mask, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       const int pos = ctr[e] + rank;
@@ -139,6 +148,8 @@ __global__ void __launch_bounds__(32) permute_assign_kernel(const int32_t* __res
       if (rank == 0) ctr[e] += __popc(peers);
       row_of[s] = pos;
       src_tok[pos] = s / k;
+    } else if (s < hi) {
+      row_of[s] = -1;  // expert id outside [0, E): the slot is left out
     }
     __syncwarp();
   }
@@ -158,8 +169,10 @@ DEVINL uint4 cvt_row_vec(uint4 v, bool to_f16) {
 
 // One warp per permuted row; copies row_bytes (multiple of 16) and sf bytes
 // (multiple of 4).  to_f16: the row holds bf16 values, written as fp16.
+// Rows past offsets[E] exist only when slots were left out; their src_tok
+// entries were never written, so a token id outside [0, T) is skipped.
 template <bool TO_F16>
-__global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __restrict__ src_tok, int S,
+__global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __restrict__ src_tok, int S, int T,
                                                              const uint8_t* __restrict__ x, int row_bytes,
                                                              const uint8_t* __restrict__ x_sf, int sf_bytes,
                                                              uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_sf) {
@@ -167,6 +180,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __re
   const int lane = threadIdx.x & 31;
   if (r >= S) return;
   const int t = __ldg(src_tok + r);
+  if (static_cast<unsigned>(t) >= static_cast<unsigned>(T)) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * row_bytes);
   uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(r) * row_bytes);
   const int nvec = row_bytes >> 4;
@@ -202,16 +216,17 @@ int permute_launch(const int32_t* idx, int T, int k, int E, const void* x_rows, 
   int32_t* base = carve.take<int32_t>(static_cast<size_t>(C) * E);
   if (!carve.fits()) return MOE_ERR_WORKSPACE;
   const size_t shbytes = static_cast<size_t>(E) * sizeof(int32_t);
-  if (C > 0) permute_count_kernel<<<C, 256, shbytes, s>>>(idx, S, E, hist);
+  unsigned int* err = device_error_word();  // NULL if the lookup failed: ids are still checked
+  if (C > 0) permute_count_kernel<<<C, 256, shbytes, s>>>(idx, S, E, hist, err);
   permute_scan_kernel<<<1, 1024, 0, s>>>(hist, C, E, base, counts, offsets);
   if (C > 0) permute_assign_kernel<<<C, 32, shbytes, s>>>(idx, S, k, E, base, row_of, src_tok);
   if (xp_rows != nullptr && S > 0) {
     const int blocks = (S + 7) / 8;
     if (to_f16)
-      permute_gather_kernel<true><<<blocks, 256, 0, s>>>(src_tok, S, static_cast<const uint8_t*>(x_rows), row_bytes,
+      permute_gather_kernel<true><<<blocks, 256, 0, s>>>(src_tok, S, T, static_cast<const uint8_t*>(x_rows), row_bytes,
                                                          x_sf, sf_row_bytes, static_cast<uint8_t*>(xp_rows), xp_sf);
     else
-      permute_gather_kernel<false><<<blocks, 256, 0, s>>>(src_tok, S, static_cast<const uint8_t*>(x_rows), row_bytes,
+      permute_gather_kernel<false><<<blocks, 256, 0, s>>>(src_tok, S, T, static_cast<const uint8_t*>(x_rows), row_bytes,
                                                           x_sf, sf_row_bytes, static_cast<uint8_t*>(xp_rows), xp_sf);
   }
   return check_launch();

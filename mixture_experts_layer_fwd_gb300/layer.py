@@ -31,6 +31,19 @@ def quantize_weights(w: torch.Tensor) -> NVFP4Tensor:
     return NVFP4Tensor(codes, sf, g)
 
 
+def _check_weight(t: Optional[torch.Tensor], name: str, shape, device=None) -> None:
+    if t is None:
+        raise ValueError(f"{name}: required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name}: expected bf16 master weights, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
 class MoELayer:
     def __init__(self, H: int, E: int, k: int, I: int, I_s: int, w13: torch.Tensor, w2: torch.Tensor,
                  ws13: Optional[torch.Tensor] = None, ws2: Optional[torch.Tensor] = None,
@@ -42,6 +55,13 @@ class MoELayer:
         SwiGLU output (g_hs for the shared expert, default g_h).
         renorm=False routes without renormalisation; shared_gate (bf16 [H])
         scales the shared expert by sigmoid(x . shared_gate)."""
+        if w_fmt not in _FMT or act_fmt not in _FMT:
+            raise ValueError(f"formats: expected 'bf16' or 'nvfp4', got {w_fmt!r}, {act_fmt!r}")
+        _check_weight(w13, "w13", (E, 2 * I, H))
+        _check_weight(w2, "w2", (E, H, I), w13.device)
+        if I_s:
+            _check_weight(ws13, "ws13", (2 * I_s, H), w13.device)
+            _check_weight(ws2, "ws2", (H, I_s), w13.device)
         self.H, self.E, self.k, self.I, self.I_s = H, E, k, I, I_s
         self.w_fmt, self.act_fmt = w_fmt, act_fmt
         self.device = w13.device
@@ -77,6 +97,8 @@ class MoELayer:
         if shared_gate is not None:
             if not I_s:
                 raise ValueError("a shared-expert gate needs a shared expert (I_s > 0)")
+            if tuple(shared_gate.shape) != (H,):
+                raise ValueError(f"shared_gate: expected shape ({H},), got {tuple(shared_gate.shape)}")
             self.shared_gate = shared_gate.to(device=self.device, dtype=torch.bfloat16).contiguous()
             c.ws_gate = self.shared_gate.data_ptr()
             self._keep.append(self.shared_gate)
