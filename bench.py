@@ -123,22 +123,45 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-def gemm_traffic_per_launch():
-    """DRAM bytes per grouped-GEMM launch at the bench workload, from the
-    committed ncu summary -- only while gemm_pair.cu is the source it was
-    taken on."""
+# The bf16 grouped-GEMM kernel's translation unit and every header it
+# includes: the kernel is "the same" only while all of them are.
+PAIR_KERNEL_SOURCES = ("mixture_experts_layer_fwd_gb300/csrc/gemm_pair.cu",
+                       "mixture_experts_layer_fwd_gb300/csrc/gemm_common.cuh",
+                       "mixture_experts_layer_fwd_gb300/csrc/nvfp4.cuh",
+                       "mixture_experts_layer_fwd_gb300/csrc/common.cuh",
+                       "mixture_experts_layer_fwd_gb300/csrc/internal.h",
+                       "include/moe_gb300.h")
+
+
+def pair_kernel_sources_hash():
+    """sha256 over the bf16 grouped-GEMM kernel's sources, in the order of
+    PAIR_KERNEL_SOURCES (None if one is missing)."""
     import hashlib
-    import re
-    prof = os.path.join(ROOT, "profiles", "grouped_gemm_pair_qwen3-235b-e32_T2048.md")
-    src = os.path.join(ROOT, "mixture_experts_layer_fwd_gb300", "csrc", "gemm_pair.cu")
+    h = hashlib.sha256()
     try:
-        text = open(prof).read()
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        for rel in PAIR_KERNEL_SOURCES:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
     except OSError:
         return None
-    m_h = re.search(r"sha256 prefix ([0-9a-f]+)", text)
+    return h.hexdigest()
+
+
+def gemm_traffic_per_launch():
+    """DRAM bytes per grouped-GEMM launch at the bench workload, from the
+    committed ncu summary -- only while the kernel's sources (the .cu and the
+    headers it includes) hash to the "sources sha256 prefix" the summary
+    states; otherwise None."""
+    import re
+    prof = os.path.join(ROOT, "profiles", "grouped_gemm_pair_qwen3-235b-e32_T2048.md")
+    try:
+        text = open(prof).read()
+    except OSError:
+        return None
+    h = pair_kernel_sources_hash()
+    m_h = re.search(r"sources sha256 prefix ([0-9a-f]{8,})", text)
     m_t = re.search(r"scales to ([0-9.]+) GB per launch", text)
-    if not (m_h and m_t) or not h.startswith(m_h.group(1)):
+    if h is None or not (m_h and m_t) or not h.startswith(m_h.group(1)):
         return None
     return float(m_t.group(1)) * 1e9
 

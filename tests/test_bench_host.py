@@ -84,17 +84,38 @@ def test_peaks_come_from_the_measured_file_else_the_fallback():
 
 
 def test_traffic_figure_tracks_the_profiled_source():
-    """The committed ncu summary of the bf16 pair kernel states the source
-    hash it was taken on and the DRAM bytes per launch scaled to the bench
-    workload; the bench reports that figure only while the source matches."""
-    t = bench.gemm_traffic_per_launch()
-    text = open(os.path.join(ROOT, "profiles", "grouped_gemm_pair_qwen3-235b-e32_T2048.md")).read()
+    """The committed ncu summary of the bf16 pair kernel gives the DRAM bytes
+    per launch scaled to the bench workload; the bench reports that figure
+    only while the summary states the hash of the kernel's current sources
+    (the .cu and every header it includes), else null."""
     import hashlib
     import re
-    h = hashlib.sha256(open(os.path.join(ROOT, "mixture_experts_layer_fwd_gb300", "csrc",
-                                         "gemm_pair.cu"), "rb").read()).hexdigest()
-    stated = re.search(r"sha256 prefix ([0-9a-f]+)", text).group(1)
-    if h.startswith(stated):
+    t = bench.gemm_traffic_per_launch()
+    text = open(os.path.join(ROOT, "profiles", "grouped_gemm_pair_qwen3-235b-e32_T2048.md")).read()
+    h = hashlib.sha256()
+    for rel in ("mixture_experts_layer_fwd_gb300/csrc/gemm_pair.cu",
+                "mixture_experts_layer_fwd_gb300/csrc/gemm_common.cuh",
+                "mixture_experts_layer_fwd_gb300/csrc/nvfp4.cuh",
+                "mixture_experts_layer_fwd_gb300/csrc/common.cuh",
+                "mixture_experts_layer_fwd_gb300/csrc/internal.h", "include/moe_gb300.h"):
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    stated = re.search(r"sources sha256 prefix ([0-9a-f]{8,})", text)
+    if stated and h.hexdigest().startswith(stated.group(1)):
         assert t == pytest.approx(float(re.search(r"scales to ([0-9.]+) GB", text).group(1)) * 1e9)
     else:
         assert t is None
+
+
+def test_every_header_the_pair_kernel_includes_is_hashed():
+    import re
+    csrc = os.path.join(ROOT, "mixture_experts_layer_fwd_gb300", "csrc")
+    seen, todo = set(), ["gemm_pair.cu"]
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.add(f)
+        for inc in re.findall(r'#include "([^"]+)"', open(os.path.join(csrc, f)).read()):
+            todo.append(os.path.relpath(os.path.normpath(os.path.join(csrc, os.path.dirname(f), inc)), csrc))
+    hashed = {os.path.relpath(os.path.join(ROOT, r), csrc) for r in bench.PAIR_KERNEL_SOURCES}
+    assert seen == hashed, (seen, hashed)
