@@ -236,50 +236,6 @@ int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue,
                      void* C, uint8_t* C_sf, const float* c_g,
                      void* stream);
 
-/* --------------------------------------- NVFP4 scales in the MMA's order
- * Not yet validated on hardware: these calls and the GEMM below compile for
- * sm_103a and pass their host-side checks, but have not run on a GPU.
- *
- * The scale factors of an NVFP4 operand rearranged into the order in which
- * the block-scaled MMA (128 rows x K = 64) reads them, so that a GEMM stage
- * fetches the scales of all its MMAs with one contiguous copy per operand.
- * A tile is 128 rows of an operand; its scales are K/64 blocks of 512 bytes,
- * one per MMA.  For row m of a tile, k-step kk and byte b:
- *   tiled[((tile * K/64 + kk) * 32 + m % 32) * 16 + 4 * (m / 32) + b]
- *       = sf[row][4 * kk + b]          (sf row-major [rows, K/16])
- * Rows past the end of a group are zero.  Tile numbering:
- *   rows in G groups (offsets [G+1], device): tile tile_base[g] + q holds rows
- *     offsets[g] + 128 q + m, with tile_base[g] = sum_{g' < g} ceil(rows_g'/128)
- *     (moe_sf_tile_bases; offsets are read as the grouped GEMM reads them)
- *   weights sf [G, N, K/16] (swiglu 0): tile g * ceil(N/128) + n holds rows
- *     128 n + m of group g
- *   weights sf [G, 2N, K/16] (swiglu 1, gate rows [0, N), up rows [N, 2N)):
- *     tile g * ceil(N/64) + n holds gate rows 64 n + m for m < 64 and up
- *     rows N + 64 n + (m - 64) for m >= 64
- * Requirements: K % 256 == 0; sf and tiled 16-byte aligned; G <= 1024 for
- * grouped rows.  Sizes (bytes) from the two size calls (0 on invalid input);
- * the grouped-rows size is an upper bound (every group's last tile whole). */
-size_t moe_sf_tiles_size(int M_total, int G, int K);
-size_t moe_sf_tiles_size_weights(int G, int N, int K, int swiglu);
-/* tile_base : int32 [G+1] device output */
-int moe_sf_tile_bases(const int32_t* offsets, int G, int M_total, int32_t* tile_base, void* stream);
-int moe_sf_retile_rows(const uint8_t* sf, int M_total, int K, const int32_t* offsets,
-                       const int32_t* tile_base, int G, uint8_t* tiled, void* stream);
-int moe_sf_retile_weights(const uint8_t* sf, int G, int N, int K, int swiglu, uint8_t* tiled,
-                          void* stream);
-
-/* moe_grouped_gemm for NVFP4 x NVFP4 with both operands' scales tiled as
- * above (A_sf_tiled: rows grouped by `offsets`, capacity
- * moe_sf_tiles_size(M_total, G, K); W_sf_tiled: weights, swiglu = epilogue
- * != STORE_BF16).  Same operands, epilogues and results as moe_grouped_gemm
- * otherwise; C_sf of SWIGLU_NVFP4 is written row-major.  The scales of a
- * stage travel by one bulk copy per operand and enter tensor memory by
- * tcgen05.cp.  Requires K % 256 == 0 and 16-byte aligned tiled buffers. */
-int moe_grouped_gemm_nvf4_tiled(int epilogue, int G, const int32_t* offsets, int M_total, int N, int K,
-                                const uint8_t* A, const uint8_t* A_sf_tiled, const float* A_g,
-                                const uint8_t* W, const uint8_t* W_sf_tiled, const float* W_g,
-                                void* C, uint8_t* C_sf, const float* c_g, void* stream);
-
 /* ----------------------------------------------------------------- combine
  * Weighted unpermute ("CuTeDSL at Perplexity", combine kernel: vectorised
  * accumulation in registers using the token positions from dispatch):

@@ -65,14 +65,6 @@ SIGNATURES = {
     "moe_grouped_gemm": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_int, c_int, c_int,
                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_void_p, c_void_p]),
-    "moe_sf_tiles_size": (c_size_t, [c_int, c_int, c_int]),
-    "moe_sf_tiles_size_weights": (c_size_t, [c_int, c_int, c_int, c_int]),
-    "moe_sf_tile_bases": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p]),
-    "moe_sf_retile_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
-    "moe_sf_retile_weights": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
-    "moe_grouped_gemm_nvf4_tiled": (c_int, [c_int, c_int, c_void_p, c_int, c_int, c_int,
-                                            c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                            c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                             c_void_p, c_void_p]),
     "moe_combine_gated": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,

@@ -254,107 +254,6 @@ def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tenso
     return (C, C_sf) if epilogue == MOE_EPI_SWIGLU_NVFP4 else C
 
 
-def moe_sf_tile_bases(offsets: torch.Tensor, M_total: int, stream=None) -> torch.Tensor:
-    """offsets int32 [G+1] -> tile_base int32 [G+1]: the first 128-row scale
-    tile of each group in the tiled layout (include/moe_gb300.h)."""
-    _dev(offsets, "offsets", dtype=torch.int32)
-    G = offsets.numel() - 1
-    tb = torch.empty(G + 1, dtype=torch.int32, device=offsets.device)
-    check(load().moe_sf_tile_bases(_ptr(offsets), G, int(M_total), _ptr(tb), _stream(stream)), "moe_sf_tile_bases")
-    return tb
-
-
-def moe_sf_retile_rows(sf: torch.Tensor, offsets: torch.Tensor, tile_base: torch.Tensor, K: int,
-                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Row-major scales uint8 [M_total, K/16] of rows grouped by `offsets` ->
-    the tiled layout (uint8, moe_sf_tiles_size bytes)."""
-    _dev(sf, "sf", dtype=torch.uint8)
-    dev = sf.device
-    M = sf.shape[0] if sf.dim() == 2 else 0
-    if sf.dim() != 2 or sf.shape[1] != K // 16:
-        raise ValueError(f"sf: expected [M_total, {K // 16}]")
-    _dev(offsets, "offsets", dtype=torch.int32, device=dev)
-    G = offsets.numel() - 1
-    _dev(tile_base, "tile_base", dtype=torch.int32, shape=(G + 1,), device=dev)
-    lib = load()
-    n = int(lib.moe_sf_tiles_size(M, G, int(K)))
-    if n == 0:
-        raise ValueError("moe_sf_tiles_size rejected (M_total, G, K)")
-    if out is None:
-        out = torch.empty(n, dtype=torch.uint8, device=dev)
-    _dev(out, "out", device=dev)
-    _at_least(out, "out", n)
-    check(lib.moe_sf_retile_rows(_ptr(sf), M, int(K), _ptr(offsets), _ptr(tile_base), G, _ptr(out),
-                                 _stream(stream)), "moe_sf_retile_rows")
-    return out
-
-
-def moe_sf_retile_weights(sf: torch.Tensor, N: int, K: int, swiglu: bool, out: Optional[torch.Tensor] = None,
-                          stream=None) -> torch.Tensor:
-    """Weight scales uint8 [G, Wn, K/16] (Wn = 2N with swiglu, else N) -> the
-    tiled layout (uint8, moe_sf_tiles_size_weights bytes)."""
-    _dev(sf, "sf", dtype=torch.uint8)
-    wn = 2 * N if swiglu else N
-    if sf.dim() != 3 or sf.shape[1] != wn or sf.shape[2] != K // 16:
-        raise ValueError(f"sf: expected [G, {wn}, {K // 16}]")
-    G = sf.shape[0]
-    lib = load()
-    n = int(lib.moe_sf_tiles_size_weights(G, int(N), int(K), int(bool(swiglu))))
-    if n == 0:
-        raise ValueError("moe_sf_tiles_size_weights rejected (G, N, K)")
-    if out is None:
-        out = torch.empty(n, dtype=torch.uint8, device=sf.device)
-    _dev(out, "out", device=sf.device)
-    _at_least(out, "out", n)
-    check(lib.moe_sf_retile_weights(_ptr(sf), G, int(N), int(K), int(bool(swiglu)), _ptr(out), _stream(stream)),
-          "moe_sf_retile_weights")
-    return out
-
-
-def moe_grouped_gemm_nvf4_tiled(epilogue: int, offsets: torch.Tensor, N: int, K: int, A: torch.Tensor,
-                                A_sf_tiled: torch.Tensor, A_g: torch.Tensor, W: torch.Tensor,
-                                W_sf_tiled: torch.Tensor, W_g: torch.Tensor, c_g=None, C=None, C_sf=None,
-                                stream=None):
-    """NVFP4 x NVFP4 grouped GEMM with both operands' scales in the tiled
-    layout (moe_sf_retile_rows / moe_sf_retile_weights)."""
-    _dev(A, "A", dtype=torch.uint8)
-    dev = A.device
-    _dev(offsets, "offsets", dtype=torch.int32, device=dev)
-    G = offsets.numel() - 1
-    M = A.shape[0]
-    swiglu = epilogue in (MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_NVFP4)
-    wn = 2 * N if swiglu else N
-    lib = load()
-    _at_least(A, "A", M * K // 2)
-    _dev(A_sf_tiled, "A_sf_tiled", device=dev)
-    _at_least(A_sf_tiled, "A_sf_tiled", int(lib.moe_sf_tiles_size(M, G, int(K))))
-    _dev(A_g, "A_g", dtype=torch.float32, device=dev)
-    _dev(W, "W", device=dev)
-    _at_least(W, "W", G * wn * K // 2)
-    _dev(W_sf_tiled, "W_sf_tiled", device=dev)
-    _at_least(W_sf_tiled, "W_sf_tiled", int(lib.moe_sf_tiles_size_weights(G, int(N), int(K), int(swiglu))))
-    _dev(W_g, "W_g", dtype=torch.float32, device=dev)
-    _at_least(W_g, "W_g", 4 * G)
-    if C is None:
-        if epilogue == MOE_EPI_SWIGLU_NVFP4:
-            C = torch.empty(M, N // 2, dtype=torch.uint8, device=dev)
-            C_sf = torch.empty(M, N // 16, dtype=torch.uint8, device=dev)
-        else:
-            C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-    _dev(C, "C", device=dev)
-    if epilogue == MOE_EPI_SWIGLU_NVFP4:
-        _at_least(C, "C", M * N // 2)
-        _dev(C_sf, "C_sf", device=dev)
-        _at_least(C_sf, "C_sf", M * N // 16)
-        _dev(c_g, "c_g", dtype=torch.float32, device=dev)
-    else:
-        _at_least(C, "C", M * N * 2)
-    check(lib.moe_grouped_gemm_nvf4_tiled(epilogue, G, _ptr(offsets), M, N, K, _ptr(A), _ptr(A_sf_tiled),
-                                          _ptr(A_g), _ptr(W), _ptr(W_sf_tiled), _ptr(W_g), _ptr(C), _ptr(C_sf),
-                                          _ptr(c_g), _stream(stream)), "moe_grouped_gemm_nvf4_tiled")
-    return (C, C_sf) if epilogue == MOE_EPI_SWIGLU_NVFP4 else C
-
-
 def moe_combine(Y: torch.Tensor, row_of: torch.Tensor, w: torch.Tensor, Ys: Optional[torch.Tensor],
                 T: int, k: int, H: int, out: Optional[torch.Tensor] = None, stream=None,
                 ys_gate: Optional[torch.Tensor] = None):
@@ -465,8 +364,7 @@ def moe_forward_host(layer_c, x_host: torch.Tensor, logits_host: torch.Tensor, o
 __all__ = ["MOE_FMT_BF16", "MOE_FMT_NVFP4", "MOE_EPI_STORE_BF16", "MOE_EPI_SWIGLU_BF16",
            "MOE_EPI_SWIGLU_NVFP4", "moe_version", "moe_sync_status", "moe_set_wait_timeout_ns",
            "moe_selftest_wait_timeout", "moe_route", "moe_permute", "moe_quant_nvfp4",
-           "moe_permute_noalloc", "moe_grouped_gemm", "moe_sf_tile_bases", "moe_sf_retile_rows",
-           "moe_sf_retile_weights", "moe_grouped_gemm_nvf4_tiled", "moe_combine", "moe_shared_gate",
+           "moe_permute_noalloc", "moe_grouped_gemm", "moe_combine", "moe_shared_gate",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_profiled", "moe_forward_host",
            "ForwardGraph"]
 

@@ -182,15 +182,6 @@ DEVINL void tma_load_4d(const void* tmap, uint64_t* bar, void* smem_dst, int x, 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
-// Plain (non-tensor) bulk copy global -> shared, completing on an mbarrier
-// as transaction bytes.  Both addresses 16-byte aligned, bytes a multiple
-// of 16.
-DEVINL void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(smem_dst)),
-               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
 DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // ---- cp.async (4-byte asynchronous copies global -> shared)

@@ -479,34 +479,9 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
   return MOE_ERR_UNSUPPORTED;
 }
 
-int grouped_gemm_launch_tiled(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
-                              const GemmProblem* sh, int shared_rows, cudaStream_t s) {
-  if (G < 1 || G > gg::MAX_G - 1 || !offsets) return MOE_ERR_INVALID_ARG;
-  if (epi < MOE_EPI_STORE_BF16 || epi > MOE_EPI_SWIGLU_NVFP4) return MOE_ERR_INVALID_ARG;
-  MOE_TRY(check_problem(epi, true, true, routed));
-  if (sh) MOE_TRY(check_problem(epi, true, true, *sh));
-  auto tiled_ok = [](const GemmProblem& P) {
-    return P.K % 256 == 0 && aligned(P.A_sf, 16) && aligned(P.W_sf, 16);
-  };
-  if (!tiled_ok(routed) || (sh && !tiled_ok(*sh))) return MOE_ERR_UNSUPPORTED;
-  if (routed.a_rows == 0) return MOE_OK;
-  return grouped_gemm_launch_nvf4_tiled(epi, routed, offsets, G, sh, shared_rows, s);
-}
-
 }  // namespace moe
 
 using namespace moe;
-
-extern "C" int moe_grouped_gemm_nvf4_tiled(int epilogue, int G, const int32_t* offsets, int M_total, int N, int K,
-                                           const uint8_t* A, const uint8_t* A_sf_tiled, const float* A_g,
-                                           const uint8_t* W, const uint8_t* W_sf_tiled, const float* W_g, void* C,
-                                           uint8_t* C_sf, const float* c_g, void* stream) {
-  if (M_total < 0) return MOE_ERR_INVALID_ARG;
-  if (epilogue < MOE_EPI_STORE_BF16 || epilogue > MOE_EPI_SWIGLU_NVFP4) return MOE_ERR_INVALID_ARG;
-  if (M_total == 0) return MOE_OK;
-  GemmProblem P{A, A_sf_tiled, A_g, M_total, W, W_sf_tiled, W_g, G, C, C_sf, c_g, N, K};
-  return grouped_gemm_launch_tiled(epilogue, P, offsets, G, nullptr, 0, static_cast<cudaStream_t>(stream));
-}
 
 extern "C" int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue, int G, const int32_t* offsets, int M_total, int N,
                                 int K, const void* A, const uint8_t* A_sf, const float* A_g, const void* W,

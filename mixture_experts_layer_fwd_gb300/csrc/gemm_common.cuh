@@ -26,7 +26,6 @@ struct Prob {
   const uint8_t* a_sf;
   const uint8_t* w_sf;
   int a_f16;         // A holds fp16 (else bf16), NVFP4-weight kernel
-  int a_sf_tiles;    // tiles the tiled A scale buffer holds (tiled-scale kernel)
 };
 
 struct Params {

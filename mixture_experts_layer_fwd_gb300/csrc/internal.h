@@ -59,19 +59,5 @@ int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t*
                               const GemmProblem* sh, int shared_rows, cudaStream_t s);
 int grouped_gemm_launch_nvf4_wide(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                                   const GemmProblem* sh, int shared_rows, cudaStream_t s);
-// Both operands NVFP4 with the scales in the MMA's tile order (sf_tiles.cu):
-// A_sf / W_sf of the problems are tiled buffers (gemm_fp4t.cu).
-int grouped_gemm_launch_nvf4_tiled(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
-                                   const GemmProblem* sh, int shared_rows, cudaStream_t s);
-// Checks the problems and launches grouped_gemm_launch_nvf4_tiled.
-int grouped_gemm_launch_tiled(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
-                              const GemmProblem* sh, int shared_rows, cudaStream_t s);
-
-// Scale factors in the MMA's tile order (sf_tiles.cu).
-size_t sf_tiles_bytes_rows(int M, int G, int K);
-int sf_tile_base_launch(const int32_t* offsets, int G, int M, int32_t* tile_base, cudaStream_t s);
-int sf_retile_rows_launch(const uint8_t* sf, int M, int K, const int32_t* offsets, const int32_t* tile_base, int G,
-                          uint8_t* tiled, cudaStream_t s);
-int sf_retile_weights_launch(const uint8_t* sf, int G, int N, int K, bool swiglu, uint8_t* tiled, cudaStream_t s);
 
 }  // namespace moe

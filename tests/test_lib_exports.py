@@ -91,33 +91,3 @@ def test_forward_layer_validation(lib):
     c.H = 4096
     c.act_fmt = L.MOE_FMT_NVFP4  # NVFP4 activations need NVFP4 weights
     assert lib.moe_forward(ctypes.byref(c), None, None, 4, None, None, 0, None) == L.MOE_ERR_UNSUPPORTED
-
-
-def test_tiled_scale_calls_check_arguments_on_the_host(lib):
-    """Sizes of the tiled scale buffers and the host-side rejections of the
-    tiled-scale calls (nothing here reaches a launch)."""
-    from mixture_experts_layer_fwd_gb300 import _lib as L
-    P = ctypes.c_void_p
-    # rows grouped: (ceil(M/128) + G) tiles of K/64 blocks of 512 bytes
-    assert lib.moe_sf_tiles_size(1000, 8, 512) == (8 + 8) * (512 // 64) * 512
-    assert lib.moe_sf_tiles_size(1000, 8, 320) == 0  # K % 256 != 0
-    assert lib.moe_sf_tiles_size(-1, 8, 512) == 0
-    # weights: G * ceil(N/128) tiles (STORE) or G * ceil(N/64) tiles (SwiGLU)
-    assert lib.moe_sf_tiles_size_weights(4, 7168, 2048, 0) == 4 * 56 * (2048 // 64) * 512
-    assert lib.moe_sf_tiles_size_weights(4, 2048, 7168, 1) == 4 * 32 * (7168 // 64) * 512
-    assert lib.moe_sf_tiles_size_weights(4, 100, 512, 0) == 4 * 1 * 8 * 512
-    assert lib.moe_sf_tile_bases(None, 4, 100, None, None) == L.MOE_ERR_INVALID_ARG
-    assert lib.moe_sf_tile_bases(P(256), 2000, 100, P(256), None) == L.MOE_ERR_UNSUPPORTED
-    assert lib.moe_sf_retile_rows(None, 0, 512, None, None, 4, None, None) == L.MOE_OK  # no rows
-    assert lib.moe_sf_retile_rows(P(256), 100, 320, P(256), P(256), 4, P(256), None) == L.MOE_ERR_UNSUPPORTED
-    assert lib.moe_sf_retile_rows(P(264), 100, 512, P(256), P(256), 4, P(256), None) == L.MOE_ERR_INVALID_ARG
-    assert lib.moe_sf_retile_weights(P(256), 4, 128, 320, 0, P(256), None) == L.MOE_ERR_UNSUPPORTED
-    assert lib.moe_sf_retile_weights(P(256), 4, 128, 512, 0, P(8), None) == L.MOE_ERR_INVALID_ARG
-
-    def gemm(M, K, sfa):
-        return lib.moe_grouped_gemm_nvf4_tiled(0, 2, P(256), M, 128, K, P(256), sfa, P(256), P(256), P(256),
-                                               P(256), P(256), None, None, None)
-    assert gemm(256, 320, P(256)) == L.MOE_ERR_UNSUPPORTED  # K % 256 != 0
-    assert gemm(256, 512, P(260)) == L.MOE_ERR_UNSUPPORTED  # tiled scales not 16-byte aligned
-    assert gemm(0, 512, P(256)) == L.MOE_OK
-    assert gemm(-1, 512, P(256)) == L.MOE_ERR_INVALID_ARG
