@@ -66,3 +66,17 @@ def test_layer_rejects_host_weights_and_unknown_formats():
 def test_missing_operand_is_named():
     with pytest.raises(ValueError, match="A: required"):
         m.moe_grouped_gemm(0, 0, 0, None, 128, 64, None, None)
+
+
+def test_every_binding_is_exported_by_the_package():
+    """What api.py binds is reachable as mixture_experts_layer_fwd_gb300.<name>,
+    and every C entry point of the header that takes tensors has a wrapper."""
+    from mixture_experts_layer_fwd_gb300 import _lib, api
+    assert set(api.__all__) <= set(m.__all__)
+    for name in api.__all__:
+        assert getattr(m, name) is getattr(api, name)
+    size_queries = {n for n in _lib.SIGNATURES if n.endswith("_workspace_size") or n.endswith("_size")}
+    handled_elsewhere = {"moe_status_string", "moe_last_cuda_error", "moe_route_ex", "moe_combine_gated",
+                         "moe_forward_graph_create", "moe_graph_launch", "moe_graph_destroy"}
+    missing = set(_lib.SIGNATURES) - set(api.__all__) - size_queries - handled_elsewhere
+    assert not missing, sorted(missing)
