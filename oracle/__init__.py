@@ -8,10 +8,10 @@ Every function is pinned by tests under tests/ (marked "not gpu") against
 brute force, closed forms, invariants, a library routine, or hand-worked
 values in tests/golden/.  No function here is "parity unpinned".
 """
-from . import nvfp4
+from . import mx, nvfp4
 from .moe import (ExpertWeights, Permutation, expert_mlp, forward, gather_rows,
                   permute, rel_frobenius, route, shared_gate, sigmoid, silu, unpermute)
 
-__all__ = ["nvfp4", "ExpertWeights", "Permutation", "expert_mlp", "forward",
+__all__ = ["mx", "nvfp4", "ExpertWeights", "Permutation", "expert_mlp", "forward",
            "gather_rows", "permute", "rel_frobenius", "route", "shared_gate",
            "sigmoid", "silu", "unpermute"]

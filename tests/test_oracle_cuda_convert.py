@@ -1,4 +1,4 @@
-"""Pins the oracle's E4M3 and E2M1 encoders to an independent implementation:
+"""Pins the oracle's E4M3, E2M1 and E8M0 codecs to an independent implementation:
 the fp32 -> FP8 (E4M3, saturating to the largest finite value) and fp32 ->
 FP4 (E2M1, round to nearest even) conversions that CUDA's cuda_fp8.h and
 cuda_fp4.h declare for host code, called from a small host program
@@ -15,7 +15,7 @@ import subprocess
 import numpy as np
 import pytest
 
-from oracle import nvfp4
+from oracle import mx, nvfp4
 
 F32 = np.float32
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,11 +31,20 @@ def converter(tmp_path_factory):
     subprocess.run([cxx, "-O1", "-std=c++17", f"-I{CUDA_INC}", os.path.join(HERE, "cuda_host", "fp_convert.cpp"),
                     "-o", exe], check=True, capture_output=True)
 
-    def run(vals: np.ndarray):
-        vals = np.ascontiguousarray(vals, dtype=F32)
-        text = "\n".join(f"{b:08x}" for b in vals.view(np.uint32).tolist()) + "\n"
-        out = subprocess.run([exe], input=text, capture_output=True, text=True, check=True).stdout.split()
-        pairs = np.array([int(t, 16) for t in out], dtype=np.int64).reshape(-1, 2)
+    def run(vals: np.ndarray, mode: str = "fp"):
+        """mode "fp": fp32 values -> (E4M3 bytes, E2M1 codes); "e8m0": fp32
+        values -> E8M0 bytes rounded toward zero; "e8m0dec": E8M0 bytes ->
+        bf16 bit patterns of their values."""
+        if mode == "e8m0dec":
+            words = np.asarray(vals, dtype=np.uint32)
+        else:
+            words = np.ascontiguousarray(vals, dtype=F32).view(np.uint32)
+        text = "\n".join(f"{b:08x}" for b in words.tolist()) + "\n"
+        out = subprocess.run([exe, mode], input=text, capture_output=True, text=True, check=True).stdout.split()
+        nums = np.array([int(t, 16) for t in out], dtype=np.int64)
+        if mode != "fp":
+            return nums
+        pairs = nums.reshape(-1, 2)
         return pairs[:, 0].astype(np.uint8), pairs[:, 1].astype(np.uint8)
 
     return run
@@ -81,3 +90,30 @@ def test_negative_values_that_round_to_zero_keep_the_sign(converter):
     _, ref = converter(vals)
     assert ref.tolist() == [8, 8, 8, 8, 0, 0, 0]
     assert nvfp4.e2m1_encode(vals).tolist() == ref.tolist()
+
+
+def test_e8m0_decode_matches_cuda_host_conversion(converter):
+    """Every E8M0 byte decodes to 2^(c - 127) (255: NaN), as CUDA's
+    __nv_cvt_e8m0_to_bf16raw does (bf16 holds 2^-127 .. 2^127 exactly)."""
+    import torch
+    codes = np.arange(256)
+    bits = converter(codes, "e8m0dec")
+    ref = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).double().numpy()
+    got = mx.e8m0_decode(codes)
+    assert np.array_equal(got[:255], ref[:255]) and np.isnan(got[255]) and np.isnan(ref[255])
+
+
+def test_shared_exponent_is_cudas_round_toward_zero_e8m0(converter):
+    """The scale exponent of a block is floor(log2(amax)) - emax: the E8M0
+    code of amax rounded toward zero (CUDA's __nv_cvt_float_to_e8m0 with
+    cudaRoundZero), minus emax, for every binade of fp32 from 2^-127 up."""
+    rng = np.random.default_rng(3)
+    k = rng.integers(-127, 128, 20000)
+    amax = np.ldexp(rng.uniform(1.0, 2.0, k.size), k).astype(F32)
+    amax = np.concatenate([amax, np.ldexp(1.0, np.arange(-127, 128)).astype(F32),
+                           np.nextafter(np.ldexp(1.0, np.arange(-126, 128)).astype(F32), F32(0))])
+    amax = amax[np.isfinite(amax) & (amax >= F32(2.0**-127))]
+    ref = converter(amax, "e8m0")
+    for fmt, emax in mx.EMAX.items():
+        e = mx.shared_exponent(amax, fmt)
+        assert np.array_equal(e, np.clip(ref - 127 - emax, -127, 127)), fmt
