@@ -69,6 +69,8 @@ extern "C" {
 /* ------------------------------------------------------------ data formats */
 #define MOE_FMT_BF16 0
 #define MOE_FMT_NVFP4 1
+#define MOE_FMT_MXFP8 2   /* E4M3 elements, one E8M0 scale per 32 (moe_quant_mx) */
+#define MOE_FMT_MXFP4 3   /* E2M1 elements, one E8M0 scale per 32 (moe_quant_mx) */
 
 /* -------------------------------------------------- grouped GEMM epilogues */
 #define MOE_EPI_STORE_BF16 0   /* C = A * W^T, rounded to bf16                        */
@@ -206,6 +208,26 @@ size_t moe_quant_nvfp4_workspace_size(int groups);
 int moe_quant_nvfp4(const uint16_t* x, int groups, int rows, int cols,
                     const float* g_in, uint8_t* codes, uint8_t* sf, float* g_out,
                     void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------- quant_mx
+ * Microscaling quantisation of bf16 rows (the pages name MXFP8, served for
+ * Qwen3-235B, and MXFP4 with abs-max over 32 elements: "Hosting Qwen on
+ * Blackwell", section "Quantização"; "CuTeDSL at Perplexity", Blackwell
+ * support).  Reading (Open Compute Project microscaling definition), per 32
+ * consecutive elements of a row:
+ *   e   = floor(log2 amax) - emax   (emax 8 for MXFP8's E4M3, 2 for MXFP4's
+ *         E2M1), clamped to [-127, 127]; -127 for an all-zero block
+ *   q_i = element_RNE_satfinite(x_i / 2^e), sign kept
+ *   scale byte = e + 127 (E8M0)
+ *   x      : bf16 [rows, cols], 16-byte aligned
+ *   fmt    : MOE_FMT_MXFP8 or MOE_FMT_MXFP4
+ *   codes  : MXFP8 uint8 [rows, cols] (8-byte aligned); MXFP4 packed uint8
+ *            [rows, cols/2] (element 2j in the low nibble; 4-byte aligned)
+ *   scales : uint8 [rows, cols/32]
+ * cols must be a multiple of 32.  No workspace, no tensor-wide scale.
+ * Not yet validated on hardware. */
+int moe_quant_mx(const uint16_t* x, int rows, int cols, int fmt, uint8_t* codes, uint8_t* scales,
+                 void* stream);
 
 /* ------------------------------------------------------------ grouped GEMM
  * Expert GEMMs over expert-contiguous rows ("Hosting Qwen on Blackwell",

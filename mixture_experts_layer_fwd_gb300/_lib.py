@@ -23,6 +23,8 @@ MOE_ERR_TIMEOUT = 5
 
 MOE_FMT_BF16 = 0
 MOE_FMT_NVFP4 = 1
+MOE_FMT_MXFP8 = 2
+MOE_FMT_MXFP4 = 3
 
 MOE_EPI_STORE_BF16 = 0
 MOE_EPI_SWIGLU_BF16 = 1
@@ -62,6 +64,7 @@ SIGNATURES = {
     "moe_quant_nvfp4_workspace_size": (c_size_t, [c_int]),
     "moe_quant_nvfp4": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_quant_mx": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_grouped_gemm": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_int, c_int, c_int,
                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_void_p, c_void_p]),

@@ -11,8 +11,8 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import (MOE_EPI_STORE_BF16, MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_NVFP4, MOE_FMT_BF16,
-                   MOE_FMT_NVFP4, check, load)
+from ._lib import (MOE_EPI_STORE_BF16, MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_NVFP4, MOE_FMT_BF16, MOE_FMT_MXFP4,
+                   MOE_FMT_MXFP8, MOE_FMT_NVFP4, check, load)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -204,6 +204,21 @@ def moe_quant_nvfp4(x: torch.Tensor, g_in: Optional[torch.Tensor] = None, stream
     return codes, sf, g
 
 
+def moe_quant_mx(x: torch.Tensor, fmt: int, stream=None):
+    """x bf16 [rows, cols] -> (codes, scales uint8 [rows, cols/32]): MXFP8
+    codes uint8 [rows, cols], MXFP4 packed codes uint8 [rows, cols/2]."""
+    _dev(x, "x", dtype=torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x: expected [rows, cols]")
+    if fmt not in (MOE_FMT_MXFP8, MOE_FMT_MXFP4):
+        raise ValueError("fmt: expected MOE_FMT_MXFP8 or MOE_FMT_MXFP4")
+    R, Cc = x.shape
+    codes = torch.empty(R, Cc if fmt == MOE_FMT_MXFP8 else Cc // 2, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(R, Cc // 32, dtype=torch.uint8, device=x.device)
+    check(load().moe_quant_mx(_ptr(x), R, Cc, int(fmt), _ptr(codes), _ptr(scales), _stream(stream)), "moe_quant_mx")
+    return codes, scales
+
+
 def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tensor, N: int, K: int,
                      A: torch.Tensor, W: torch.Tensor, A_sf=None, A_g=None, W_sf=None, W_g=None,
                      c_g=None, C=None, C_sf=None, stream=None):
@@ -361,7 +376,7 @@ def moe_forward_host(layer_c, x_host: torch.Tensor, logits_host: torch.Tensor, o
     return out_host
 
 
-__all__ = ["MOE_FMT_BF16", "MOE_FMT_NVFP4", "MOE_EPI_STORE_BF16", "MOE_EPI_SWIGLU_BF16",
+__all__ = ["MOE_FMT_BF16", "MOE_FMT_NVFP4", "MOE_FMT_MXFP8", "MOE_FMT_MXFP4", "moe_quant_mx", "MOE_EPI_STORE_BF16", "MOE_EPI_SWIGLU_BF16",
            "MOE_EPI_SWIGLU_NVFP4", "moe_version", "moe_sync_status", "moe_set_wait_timeout_ns",
            "moe_selftest_wait_timeout", "moe_route", "moe_permute", "moe_quant_nvfp4",
            "moe_permute_noalloc", "moe_grouped_gemm", "moe_combine", "moe_shared_gate",

@@ -91,3 +91,14 @@ def test_forward_layer_validation(lib):
     c.H = 4096
     c.act_fmt = L.MOE_FMT_NVFP4  # NVFP4 activations need NVFP4 weights
     assert lib.moe_forward(ctypes.byref(c), None, None, 4, None, None, 0, None) == L.MOE_ERR_UNSUPPORTED
+
+
+def test_quant_mx_checks_arguments_on_the_host(lib):
+    from mixture_experts_layer_fwd_gb300 import _lib as L
+    P = ctypes.c_void_p
+    assert lib.moe_quant_mx(None, 0, 64, L.MOE_FMT_MXFP8, None, None, None) == L.MOE_OK  # no rows
+    assert lib.moe_quant_mx(P(256), 4, 48, L.MOE_FMT_MXFP8, P(256), P(256), None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_quant_mx(P(256), 4, 64, L.MOE_FMT_NVFP4, P(256), P(256), None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_mx(P(264), 4, 64, L.MOE_FMT_MXFP4, P(256), P(256), None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_mx(P(256), 4, 64, L.MOE_FMT_MXFP8, P(260), P(256), None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_mx(P(256), -1, 64, L.MOE_FMT_MXFP8, P(256), P(256), None) == L.MOE_ERR_INVALID_ARG
