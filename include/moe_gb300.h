@@ -118,7 +118,8 @@ int moe_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
  *                          are ordered by ascending expert id
  *   w      : fp32 [T, k]   w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the
  *                          k chosen logits (= softmax over E renormalised)
- * One warp per token.  Supports 1 <= k <= min(E, 32), 1 <= E <= 1024. */
+ * One warp per token.  Supports 1 <= k <= min(E, 32), 1 <= E <= 1024,
+ * T < 2^27. */
 int moe_route(const float* logits, int T, int E, int k,
               int32_t* idx, float* w, void* stream);
 
@@ -157,7 +158,7 @@ int moe_route_ex(const float* logits, int T, int E, int k, int renorm,
  *   xp_sf    : [T*k, sf_row_bytes] permuted scale rows (NULL if x_sf is NULL)
  * row_bytes must be a positive multiple of 16; sf_row_bytes a positive
  * multiple of 4 (when x_sf is given); pointers 16-byte aligned.
- * E <= 4096.  Workspace: moe_permute_workspace_size(T, k, E). */
+ * E <= 4096, T*k < 2^27.  Workspace: moe_permute_workspace_size(T, k, E). */
 size_t moe_permute_workspace_size(int T, int k, int E);
 int moe_permute(const int32_t* idx, int T, int k, int E,
                 const void* x_rows, int row_bytes,
@@ -288,7 +289,7 @@ int moe_combine_gated(const uint16_t* Y, const int32_t* row_of, const float* w,
  *   x    : bf16 [T, H] activations (before any quantisation)
  *   g    : bf16 [H]    gate vector
  *   gate : fp32 [T]
- * H must be a multiple of 8; x and g 16-byte aligned. */
+ * H must be a multiple of 8, T < 2^27; x and g 16-byte aligned. */
 int moe_shared_gate(const uint16_t* x, const uint16_t* g, int T, int H,
                     float* gate, void* stream);
 
@@ -332,7 +333,7 @@ size_t moe_forward_workspace_size(const moe_layer* L, int T);
  *   logits : fp32 [T, E]
  *   out    : bf16 [T, H]
  * Constraints: those of each stage (H % 64 == 0, I % 64 == 0, I_s % 64 == 0,
- * k <= 32, E <= 1024). */
+ * k <= 32, E <= 1024, T*k < 2^27). */
 int moe_forward(const moe_layer* L, const uint16_t* x, const float* logits, int T,
                 uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 

@@ -155,6 +155,7 @@ extern "C" int moe_combine(const uint16_t* Y, const int32_t* row_of, const float
 extern "C" int moe_shared_gate(const uint16_t* x, const uint16_t* g, int T, int H, float* gate, void* stream) {
   if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
   if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T >= (1 << 27)) return MOE_ERR_UNSUPPORTED;  // one warp per token: 32 * T threads in 32 bits
   if (T == 0) return MOE_OK;
   if (!x || !g || !gate) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(g, 16) || !aligned(gate, 4)) return MOE_ERR_INVALID_ARG;

@@ -142,7 +142,8 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
   if (T == 0) return MOE_OK;
   if (!x || !logits || !out || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(logits, 4) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
-  if (static_cast<long long>(T) * L->k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  // one warp per routed row in the permutation (32 * T*k threads in 32 bits)
+  if (static_cast<long long>(T) * L->k >= (1ll << 27)) return MOE_ERR_UNSUPPORTED;
   FwdBufs b;
   if (carve(L, T, ws, ws_bytes, &b) > ws_bytes) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -247,7 +247,8 @@ extern "C" int moe_permute(const int32_t* idx, int T, int k, int E, const void* 
                            size_t ws_bytes, void* stream) {
   if (T < 0 || k < 1 || E < 1) return MOE_ERR_INVALID_ARG;
   if (E > kMaxExperts || k > E) return MOE_ERR_UNSUPPORTED;
-  if (static_cast<long long>(T) * k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  // the row copy runs one warp per routed row (32 * T*k threads in 32 bits)
+  if (static_cast<long long>(T) * k >= (1ll << 27)) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!idx || !row_of || !src_tok)) return MOE_ERR_INVALID_ARG;
   if (xp_rows != nullptr) {

@@ -93,6 +93,7 @@ extern "C" int moe_route_ex(const float* logits, int T, int E, int k, int renorm
                             void* stream) {
   if (T < 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
   if (k > E || k > 32 || E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (T >= (1 << 27)) return MOE_ERR_UNSUPPORTED;  // one warp per token: 32 * T threads in 32 bits
   if (T == 0) return MOE_OK;
   if (!logits || !idx || !w) return MOE_ERR_INVALID_ARG;
   if (!aligned(logits, 4) || !aligned(idx, 4) || !aligned(w, 4)) return MOE_ERR_INVALID_ARG;

@@ -102,3 +102,15 @@ def test_quant_mx_checks_arguments_on_the_host(lib):
     assert lib.moe_quant_mx(P(264), 4, 64, L.MOE_FMT_MXFP4, P(256), P(256), None) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_mx(P(256), 4, 64, L.MOE_FMT_MXFP8, P(260), P(256), None) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_mx(P(256), -1, 64, L.MOE_FMT_MXFP8, P(256), P(256), None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_sizes_past_the_32_bit_thread_index_are_rejected(lib):
+    """One warp per token (routing, shared gate) or per routed row
+    (permutation, layer): 32 * rows threads must stay below 2^32."""
+    from mixture_experts_layer_fwd_gb300 import _lib as L
+    P = ctypes.c_void_p
+    big = 1 << 27
+    assert lib.moe_route(P(256), big, 8, 2, P(256), P(256), None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_shared_gate(P(256), P(256), big, 256, P(256), None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_permute(P(256), big // 4, 4, 8, None, 0, None, 0, P(256), P(256), P(256), P(256), None, None,
+                           P(256), 1 << 40, None) == L.MOE_ERR_UNSUPPORTED
