@@ -323,7 +323,8 @@ typedef struct {
   const uint16_t* ws_gate;
 } moe_layer;
 
-/* Workspace bytes moe_forward needs for T tokens (0 on invalid layer). */
+/* Workspace bytes moe_forward needs for T tokens (0 on an invalid layer or
+ * a T that moe_forward rejects). */
 size_t moe_forward_workspace_size(const moe_layer* L, int T);
 
 /* The whole layer: route -> (NVFP4 activation quantisation) -> permute ->

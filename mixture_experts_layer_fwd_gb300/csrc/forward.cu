@@ -108,6 +108,7 @@ using namespace moe;
 
 extern "C" size_t moe_forward_workspace_size(const moe_layer* L, int T) {
   if (validate_layer(L) != MOE_OK || T < 0) return 0;
+  if (static_cast<long long>(T) * L->k >= (1ll << 27)) return 0;  // moe_forward rejects it
   FwdBufs b;
   return carve(L, T, nullptr, 0, &b);
 }

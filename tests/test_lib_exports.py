@@ -86,6 +86,7 @@ def test_forward_layer_validation(lib):
     n = lib.moe_forward_workspace_size(ctypes.byref(c), 256)
     # Xp + Y dominate: 2 * T*k*H*2 bytes
     assert n >= 2 * 256 * 8 * 4096 * 2
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), (1 << 27) // 8) == 0  # T*k past the limit
     c.H = 4000
     assert lib.moe_forward_workspace_size(ctypes.byref(c), 256) == 0
     c.H = 4096
