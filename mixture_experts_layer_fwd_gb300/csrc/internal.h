@@ -59,5 +59,9 @@ int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t*
                               const GemmProblem* sh, int shared_rows, cudaStream_t s);
 int grouped_gemm_launch_nvf4_wide(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                                   const GemmProblem* sh, int shared_rows, cudaStream_t s);
+// Both operands MXFP4 (E2M1 codes, E8M0 scales per 32), K % 512 == 0, bf16
+// epilogues (gemm_mxf4.cu).
+int grouped_gemm_launch_mxf4(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
+                             const GemmProblem* sh, int shared_rows, cudaStream_t s);
 
 }  // namespace moe
