@@ -115,3 +115,18 @@ def test_sizes_past_the_32_bit_thread_index_are_rejected(lib):
     assert lib.moe_shared_gate(P(256), P(256), big, 256, P(256), None) == L.MOE_ERR_UNSUPPORTED
     assert lib.moe_permute(P(256), big // 4, 4, 8, None, 0, None, 0, P(256), P(256), P(256), P(256), None, None,
                            P(256), 1 << 40, None) == L.MOE_ERR_UNSUPPORTED
+
+
+def test_mxfp4_grouped_gemm_checks_arguments_on_the_host(lib):
+    from mixture_experts_layer_fwd_gb300 import _lib as L
+    P = ctypes.c_void_p
+    MX, NV = L.MOE_FMT_MXFP4, L.MOE_FMT_NVFP4
+
+    def gemm(a_fmt, w_fmt, epi, K, sf=P(256)):
+        return lib.moe_grouped_gemm(a_fmt, w_fmt, epi, 2, P(256), 256, 128, K, P(256), sf, None, P(256), sf, None,
+                                    P(256), None, None, None)
+    assert gemm(MX, NV, 0, 512) == L.MOE_ERR_UNSUPPORTED     # both operands MXFP4 or neither
+    assert gemm(MX, MX, 2, 512) == L.MOE_ERR_UNSUPPORTED     # bf16 epilogues only
+    assert gemm(MX, MX, 0, 768) == L.MOE_ERR_UNSUPPORTED     # K % 512 != 0
+    assert gemm(MX, MX, 0, 512, sf=P(264)) == L.MOE_ERR_INVALID_ARG  # scales not 16-byte aligned
+    assert gemm(MX, MX, 0, 512, sf=None) == L.MOE_ERR_INVALID_ARG
