@@ -243,10 +243,11 @@ int moe_quant_mx(const uint16_t* x, int rows, int cols, int fmt, uint8_t* codes,
  * [G, Wn, K/16], W_g [G]); Wn = N (STORE) or 2N (SWIGLU).  Scale pointers
  * (A_g, W_g, c_g) are device pointers; pass NULL for bf16 operands.
  * SWIGLU_NVFP4 writes C = codes [M_total, N/2] and C_sf [M_total, N/16].
- * MXFP4 (a_fmt = w_fmt = MOE_FMT_MXFP4; not yet validated on hardware):
- * codes as NVFP4, scales E8M0 [.., K/32] (moe_quant_mx), no global scales
- * (A_g, W_g, c_g ignored); STORE_BF16 and SWIGLU_BF16 only; K % 512 == 0
- * and 16-byte aligned scale arrays.
+ * MX formats (a_fmt = w_fmt; not yet validated on hardware), scales E8M0
+ * [.., K/32] (moe_quant_mx), no global scales (A_g, W_g, c_g ignored),
+ * STORE_BF16 and SWIGLU_BF16 only:
+ *   MOE_FMT_MXFP4: codes as NVFP4; K % 512 == 0, 16-byte aligned scales
+ *   MOE_FMT_MXFP8: E4M3 bytes [.., K]; K % 256 == 0, 8-byte aligned scales
  * The kernel is persistent (one CTA per SM), reads offsets on the device,
  * stages tiles with TMA into shared memory, and runs tcgen05 MMAs with
  * fp32 accumulators in tensor memory.

@@ -238,8 +238,8 @@ def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tenso
         _at_least(A_sf, "A_sf", M * K // 16)
         _dev(A_g, "A_g", dtype=torch.float32, device=dev)
         _at_least(A_g, "A_g", 4)
-    elif a_fmt == MOE_FMT_MXFP4:
-        _at_least(A, "A", M * K // 2)
+    elif a_fmt in (MOE_FMT_MXFP4, MOE_FMT_MXFP8):
+        _at_least(A, "A", M * K // (2 if a_fmt == MOE_FMT_MXFP4 else 1))
         _dev(A_sf, "A_sf", device=dev)
         _at_least(A_sf, "A_sf", M * K // 32)
     else:
@@ -250,8 +250,8 @@ def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tenso
         _at_least(W_sf, "W_sf", G * wn * K // 16)
         _dev(W_g, "W_g", dtype=torch.float32, device=dev)
         _at_least(W_g, "W_g", 4 * G)
-    elif w_fmt == MOE_FMT_MXFP4:
-        _at_least(W, "W", G * wn * K // 2)
+    elif w_fmt in (MOE_FMT_MXFP4, MOE_FMT_MXFP8):
+        _at_least(W, "W", G * wn * K // (2 if w_fmt == MOE_FMT_MXFP4 else 1))
         _dev(W_sf, "W_sf", device=dev)
         _at_least(W_sf, "W_sf", G * wn * K // 32)
     else:

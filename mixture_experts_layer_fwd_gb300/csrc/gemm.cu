@@ -433,13 +433,16 @@ static int check_problem(int epi, bool a4, bool w4, const GemmProblem& P) {
 // Launches one persistent grouped GEMM over the routed problem (G groups,
 // device offsets) plus, when `sh` is non-null, the shared-expert problem as
 // one more group of `shared_rows` rows.
-// MXFP4 operands: E2M1 codes with one E8M0 scale per 32 elements, no
-// global scales; the kernel stages 16 scale bytes per row by TMA.
-static int check_problem_mx(const GemmProblem& P) {
+// MX operands: E2M1 codes (MXFP4) or E4M3 bytes (MXFP8) with one E8M0 scale
+// per 32 elements, no global scales.  The MXFP4 kernel stages 16 scale bytes
+// per row by TMA (K % 512, 16-byte aligned scales); the MXFP8 kernel loads 8
+// per row directly (K % 256, 8-byte aligned scales).
+static int check_problem_mx(const GemmProblem& P, bool fp8) {
   if (P.N <= 0 || P.K <= 0 || P.a_rows < 0 || P.groups < 1) return MOE_ERR_INVALID_ARG;
-  if (P.K % 512 != 0 || P.N % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  if (P.K % (fp8 ? 256 : 512) != 0 || P.N % 32 != 0) return MOE_ERR_UNSUPPORTED;
   if (!P.A || !P.W || !P.C || !P.A_sf || !P.W_sf) return MOE_ERR_INVALID_ARG;
-  if (!aligned(P.A, 16) || !aligned(P.W, 16) || !aligned(P.C, 16) || !aligned(P.A_sf, 16) || !aligned(P.W_sf, 16))
+  const int sfa = fp8 ? 8 : 16;
+  if (!aligned(P.A, 16) || !aligned(P.W, 16) || !aligned(P.C, 16) || !aligned(P.A_sf, sfa) || !aligned(P.W_sf, sfa))
     return MOE_ERR_INVALID_ARG;
   if (static_cast<long long>(P.groups) * 2 * P.N >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -449,12 +452,14 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
                         const GemmProblem* sh, int shared_rows, cudaStream_t s) {
   const bool a4 = a_fmt == MOE_FMT_NVFP4, w4 = w_fmt == MOE_FMT_NVFP4;
   if (G < 1 || G > gg::MAX_G - 1 || !offsets) return MOE_ERR_INVALID_ARG;
-  if (a_fmt == MOE_FMT_MXFP4 || w_fmt == MOE_FMT_MXFP4) {
+  const bool mx8 = a_fmt == MOE_FMT_MXFP8 || w_fmt == MOE_FMT_MXFP8;
+  if (mx8 || a_fmt == MOE_FMT_MXFP4 || w_fmt == MOE_FMT_MXFP4) {
     if (a_fmt != w_fmt) return MOE_ERR_UNSUPPORTED;
     if (epi != MOE_EPI_STORE_BF16 && epi != MOE_EPI_SWIGLU_BF16) return MOE_ERR_UNSUPPORTED;
-    MOE_TRY(check_problem_mx(routed));
-    if (sh) MOE_TRY(check_problem_mx(*sh));
+    MOE_TRY(check_problem_mx(routed, mx8));
+    if (sh) MOE_TRY(check_problem_mx(*sh, mx8));
     if (routed.a_rows == 0) return MOE_OK;
+    if (mx8) return grouped_gemm_launch_mxf8(epi, routed, offsets, G, sh, shared_rows, s);
     return grouped_gemm_launch_mxf4(epi, routed, offsets, G, sh, shared_rows, s);
   }
   if ((epi < MOE_EPI_STORE_BF16 || epi > MOE_EPI_SWIGLU_NVFP4) && epi != kEpiSwigluF16) return MOE_ERR_INVALID_ARG;

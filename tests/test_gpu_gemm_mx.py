@@ -1,9 +1,10 @@
-"""MXFP4 x MXFP4 grouped GEMM (moe_grouped_gemm with MOE_FMT_MXFP4) against
-the fp64 product of the oracle's dequantised operands (oracle/mx.py): ragged
-and empty groups, both bf16 epilogues, a one-group one-stage case first
-(the smallest check of the block-scale descriptor and byte selection).
+"""MXFP4 x MXFP4 and MXFP8 x MXFP8 grouped GEMMs (moe_grouped_gemm with
+MOE_FMT_MXFP4 / MOE_FMT_MXFP8) against the fp64 product of the oracle's
+dequantised operands (oracle/mx.py): ragged and empty groups, both bf16
+epilogues, a one-group one-stage case first (the smallest check of the
+block-scale descriptor and byte selection).
 
-The kernel has not run on a GPU yet, so the module runs only when
+The kernels have not run on a GPU yet, so the module runs only when
 MOE_RUN_UNVALIDATED=1 is set."""
 import os
 
@@ -20,7 +21,7 @@ pytestmark = [pytest.mark.gpu,
                                  reason="MXFP4 GEMM not yet run on a GPU; opt in with MOE_RUN_UNVALIDATED=1")]
 
 DEV = "cuda"
-MXFP4 = 3
+FMT = {"mxfp8": 2, "mxfp4": 3}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,26 +41,31 @@ def _ref(A, W, offs, swiglu, N):
     return out
 
 
-@pytest.mark.parametrize("epi,N,K,counts", [
-    (0, 128, 512, [128]),                       # one tile, one stage
-    (0, 448, 1024, [0, 1, 127, 129, 300, 0, 40]),
-    (1, 256, 1536, [300, 0, 513, 257, 64, 130]),
-    (1, 192, 512, [7, 0, 260]),
+@pytest.mark.parametrize("fmt,epi,N,K,counts", [
+    ("mxfp4", 0, 128, 512, [128]),              # one tile, one stage
+    ("mxfp4", 0, 448, 1024, [0, 1, 127, 129, 300, 0, 40]),
+    ("mxfp4", 1, 256, 1536, [300, 0, 513, 257, 64, 130]),
+    ("mxfp4", 1, 192, 512, [7, 0, 260]),
+    ("mxfp8", 0, 128, 256, [128]),              # one tile, one stage
+    ("mxfp8", 0, 448, 768, [0, 1, 127, 129, 300, 0, 40]),
+    ("mxfp8", 1, 256, 1280, [300, 0, 513, 257, 64, 130]),
+    ("mxfp8", 1, 192, 256, [7, 0, 260]),
 ])
-def test_grouped_gemm_mxfp4(epi, N, K, counts):
+def test_grouped_gemm_mx(fmt, epi, N, K, counts):
     import mixture_experts_layer_fwd_gb300 as m
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     M, G = int(offs[-1]), len(counts)
     wn = N if epi == 0 else 2 * N
     g = torch.Generator().manual_seed(N + K + epi)
     x = (torch.randn(M, K, generator=g) * torch.exp(torch.randn(M, 1, generator=g))).numpy()
-    Aq, As = mx.quantize(x, "mxfp4")
-    Wq, Ws = zip(*[mx.quantize((torch.randn(wn, K, generator=g) * 0.02).numpy(), "mxfp4") for _ in range(G)])
+    Aq, As = mx.quantize(x, fmt)
+    Wq, Ws = zip(*[mx.quantize((torch.randn(wn, K, generator=g) * 0.02).numpy(), fmt) for _ in range(G)])
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
-    C = m.moe_grouped_gemm(MXFP4, MXFP4, epi, t(offs), N, K, t(Aq), t(np.stack(Wq)), A_sf=t(As), W_sf=t(np.stack(Ws)))
+    C = m.moe_grouped_gemm(FMT[fmt], FMT[fmt], epi, t(offs), N, K, t(Aq), t(np.stack(Wq)), A_sf=t(As),
+                           W_sf=t(np.stack(Ws)))
     assert m.moe_sync_status() == 0
-    Ad = mx.dequantize(Aq, As, "mxfp4")
-    Wd = np.stack([mx.dequantize(q, s, "mxfp4") for q, s in zip(Wq, Ws)])
+    Ad = mx.dequantize(Aq, As, fmt)
+    Wd = np.stack([mx.dequantize(q, s, fmt) for q, s in zip(Wq, Ws)])
     ref = _ref(Ad, Wd, offs, epi == 1, N)
     got = C.float().cpu().numpy()
     err = oracle.rel_frobenius(got, ref)

@@ -130,3 +130,7 @@ def test_mxfp4_grouped_gemm_checks_arguments_on_the_host(lib):
     assert gemm(MX, MX, 0, 768) == L.MOE_ERR_UNSUPPORTED     # K % 512 != 0
     assert gemm(MX, MX, 0, 512, sf=P(264)) == L.MOE_ERR_INVALID_ARG  # scales not 16-byte aligned
     assert gemm(MX, MX, 0, 512, sf=None) == L.MOE_ERR_INVALID_ARG
+    M8 = L.MOE_FMT_MXFP8
+    assert gemm(M8, MX, 0, 512) == L.MOE_ERR_UNSUPPORTED
+    assert gemm(M8, M8, 0, 320) == L.MOE_ERR_UNSUPPORTED     # K % 256 != 0
+    assert gemm(M8, M8, 0, 256, sf=P(260)) == L.MOE_ERR_INVALID_ARG  # scales not 8-byte aligned
