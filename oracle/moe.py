@@ -135,7 +135,8 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 
 def expert_mlp(a: np.ndarray, w13: np.ndarray, w2: np.ndarray,
-               h_quant_g: Optional[np.float32] = None) -> np.ndarray:
+               h_quant_g: Optional[np.float32] = None,
+               h_quant: Optional[Callable[[np.ndarray], np.ndarray]] = None) -> np.ndarray:
     """One expert on a batch of rows.
 
     a   : fp64 [n, H]   input rows (already dequantised)
@@ -144,6 +145,8 @@ def expert_mlp(a: np.ndarray, w13: np.ndarray, w2: np.ndarray,
     h_quant_g : when given (NVFP4-activation path), the SwiGLU output h is
         rounded to fp32 and passed through NVFP4 quantisation with this global
         scale (blocks of 16 along I) before the down projection.
+    h_quant : when given (the MX layers, oracle.mx.h_quant), a function that
+        takes h (fp64 [n, I]) to the values the down projection sees.
     Returns fp64 [n, H].
     """
     I = w13.shape[0] // 2
@@ -153,6 +156,8 @@ def expert_mlp(a: np.ndarray, w13: np.ndarray, w2: np.ndarray,
     if h_quant_g is not None:
         q, s, _ = nvfp4.quantize(h.astype(F32), F32(h_quant_g))
         h = nvfp4.dequantize(q, s, F32(h_quant_g))
+    if h_quant is not None:
+        h = h_quant(h)
     return h @ w2.T
 
 
@@ -189,7 +194,9 @@ def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
             hs_quant_g: Optional[np.float32] = None,
             renorm: bool = True,
             shared_g: Optional[np.ndarray] = None,
-            x_gate: Optional[np.ndarray] = None):
+            x_gate: Optional[np.ndarray] = None,
+            h_quant: Optional[Callable[[np.ndarray], np.ndarray]] = None,
+            hs_quant: Optional[Callable[[np.ndarray], np.ndarray]] = None):
     """Layer output for the given tokens (all tokens when `tokens` is None).
 
     x_deq   : fp64 [T, H] the activations as the experts see them (bf16 values,
@@ -202,6 +209,8 @@ def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
     renorm  : False selects the router without renormalisation (see route)
     shared_g: gate vector [H] of the shared expert (None: ungated, weight 1);
               x_gate: the activations the gate sees ([T, H]; default x_deq)
+    h_quant / hs_quant: the step between SwiGLU and down projection of the
+              routed / shared experts on the MX layers (see expert_mlp)
     """
     x_deq = np.asarray(x_deq, dtype=np.float64)
     T, H = x_deq.shape
@@ -219,12 +228,12 @@ def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
             continue
         W = get_expert(e)
         src = perm.src_tok[rows]
-        y = expert_mlp(x_deq[src], W.w13, W.w2, h_quant_g)
+        y = expert_mlp(x_deq[src], W.w13, W.w2, h_quant_g, h_quant)
         for r, t, yr in zip(rows, src, y):
             j = int(np.nonzero(perm.row_of[t] == r)[0][0])
             out[pos[int(t)]] += w[t, j] * yr
     if shared is not None:
-        ys = expert_mlp(x_deq[toks], shared.w13, shared.w2, hs_quant_g)
+        ys = expert_mlp(x_deq[toks], shared.w13, shared.w2, hs_quant_g, hs_quant)
         if shared_g is not None:
             xg = x_deq if x_gate is None else np.asarray(x_gate, np.float64)
             ys = ys * shared_gate(xg[toks], shared_g)[:, None]

@@ -98,3 +98,26 @@ def dequantize(codes: np.ndarray, scales: np.ndarray, fmt: str) -> np.ndarray:
     rows, cols = vals.shape
     sc = e8m0_decode(scales)[:, :, None]
     return (vals.reshape(rows, cols // BLOCK, BLOCK) * sc).reshape(rows, cols)
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 -> bf16 (round to nearest even, torch's cast) -> fp64."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(np.asarray(v, dtype=np.float64).astype(F32)))
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def fake_quant(v: np.ndarray, fmt: str) -> np.ndarray:
+    """Values (fp64, last dimension a multiple of 32) through the MX codec
+    along the last dimension: the decoded values, fp64."""
+    v = np.asarray(v, dtype=np.float64)
+    q, s = quantize(v.reshape(-1, v.shape[-1]).astype(F32), fmt)
+    return dequantize(q, s, fmt).reshape(v.shape)
+
+
+def h_quant(fmt: str):
+    """The MX layers' step between the SwiGLU and the down projection.  The
+    pages leave it open; reading taken: the gate/up GEMM stores h in bf16
+    (round to nearest even) and h is quantised from there, in blocks of 32
+    along I, like the activations."""
+    return lambda h: fake_quant(round_bf16(h), fmt)

@@ -126,3 +126,67 @@ def test_blocks_are_independent_and_nibbles_ordered():
 def test_unknown_format_is_rejected():
     with pytest.raises(ValueError):
         mx.quantize(np.zeros((1, 32), F32), "mxfp6")
+
+
+# ------------------------------------------------ the MX layers' h step ----
+def _h_probe(h_values):
+    """Weights that make h = h_values for the input row e_0: gate = 50
+    (silu(50) == 50 in fp64), up_i = h_i / 50, down = identity."""
+    I = len(h_values)
+    a = np.eye(I)[:1]
+    w13 = np.zeros((2 * I, I))
+    w13[:I, 0] = 50.0
+    w13[I:, 0] = np.asarray(h_values, np.float64) / 50.0
+    return a, w13, np.eye(I)
+
+
+def test_mxfp4_h_step_hand_worked():
+    """Block amax 6 -> scale 2^0: h is rounded to the E2M1 grid itself after
+    its bf16 rounding (1.6 -> 1.6015625 -> 1.5, -5.1 -> -5.09375 -> -6)."""
+    from oracle.moe import expert_mlp
+    h = [6.0, 1.25, 3.5, 5.0, 0.25, 2.5, -0.8, 1.6, -4.4, 0.3, 0.0, 2.9, -5.1, 0.7, 1.9, 3.2] + [0.0] * 16
+    want = [6.0, 1.0, 4.0, 4.0, 0.0, 2.0, -1.0, 1.5, -4.0, 0.5, 0.0, 3.0, -6.0, 0.5, 2.0, 3.0] + [0.0] * 16
+    a, w13, w2 = _h_probe(h)
+    y = expert_mlp(a, w13, w2, h_quant=mx.h_quant("mxfp4"))[0]
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-12)
+
+
+def test_mxfp8_h_step_hand_worked():
+    """Block amax 448 -> scale 2^0: E4M3 grid, ties to the even code (17 ->
+    16, 19 -> 20, 0.0068359375 = 3.5 * 2^-9 -> 4 * 2^-9)."""
+    from oracle.moe import expert_mlp
+    h = [448.0, 17.0, 19.0, -240.0, 3.5 * 2.0**-9] + [1.0] * 27
+    want = [448.0, 16.0, 20.0, -240.0, 4 * 2.0**-9] + [1.0] * 27
+    a, w13, w2 = _h_probe(h)
+    y = expert_mlp(a, w13, w2, h_quant=mx.h_quant("mxfp8"))[0]
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-12)
+
+
+def test_h_step_rounds_to_bf16_first():
+    """1.2500001 is 1.25 in bf16, a tie between E2M1's 1 and 1.5 that goes to
+    the even code 1; quantising the fp32 value directly would give 1.5."""
+    from oracle.moe import expert_mlp
+    h = [6.0, 1.2500001] + [0.0] * 30
+    a, w13, w2 = _h_probe(h)
+    y = expert_mlp(a, w13, w2, h_quant=mx.h_quant("mxfp4"))[0]
+    assert y[1] == 1.0
+    assert mx.fake_quant(np.array([h]), "mxfp4")[0, 1] == 1.5
+
+
+def test_forward_applies_the_h_step_to_routed_and_shared_experts():
+    """forward hands h_quant to every routed expert and hs_quant to the
+    shared one: zeroing h in either removes exactly that part."""
+    from oracle.moe import ExpertWeights, forward
+    rng = np.random.default_rng(2)
+    T, H, E, k, I = 5, 32, 4, 2, 32
+    experts = [ExpertWeights(rng.standard_normal((2 * I, H)) * 0.1, rng.standard_normal((H, I)) * 0.1)
+               for _ in range(E)]
+    shared = ExpertWeights(rng.standard_normal((2 * I, H)) * 0.1, rng.standard_normal((H, I)) * 0.1)
+    x = rng.standard_normal((T, H))
+    logits = rng.standard_normal((T, E)).astype(F32)
+    zero = lambda h: 0.0 * h
+    full, *_ = forward(x, logits, k, E, lambda e: experts[e], shared)
+    routed_only, *_ = forward(x, logits, k, E, lambda e: experts[e], shared, hs_quant=zero)
+    shared_only, *_ = forward(x, logits, k, E, lambda e: experts[e], shared, h_quant=zero)
+    assert np.abs(shared_only).max() > 0 and np.abs(routed_only).max() > 0
+    np.testing.assert_allclose(routed_only + shared_only, full, rtol=1e-12, atol=1e-12)
