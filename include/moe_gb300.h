@@ -309,6 +309,13 @@ int moe_shared_gate(const uint16_t* x, const uint16_t* g, int T, int H,
  *                  scale over x) before dispatch, and the SwiGLU output h is
  *                  quantised to NVFP4 with the caller's global scales
  *                  *g_h (routed) and *g_hs (shared) before the down GEMM.
+ *   MX layers (w_fmt = act_fmt = MOE_FMT_MXFP4 or MOE_FMT_MXFP8; not yet
+ *                  validated on hardware): codes as moe_quant_mx writes them
+ *                  (w13 [E, 2I, H or H/2], w2 [E, H, I or I/2]), scales E8M0
+ *                  [.., K/32], no global scales (*_g, g_h, g_hs ignored); x
+ *                  and h are quantised the same way inside the layer, h from
+ *                  its bf16 value.  H, I, I_s multiples of 512 (MXFP4) or 256
+ *                  (MXFP8).
  * I_s = 0 means no shared expert.
  * Variants (zero-initialised fields keep the default layer):
  *   no_renorm != 0 : route without renormalisation (moe_route_ex, renorm 0)

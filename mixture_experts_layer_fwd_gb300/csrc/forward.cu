@@ -36,13 +36,36 @@ struct FwdBufs {
   uint16_t* Y;
   uint16_t* Ys;
   float* gate;  // shared-expert gate per token (gated layers)
+  // MX layers: h (bf16, in `h` / `hs`) quantised for the down projection
+  uint8_t* hq;
+  uint8_t* hq_sf;
+  uint8_t* hsq;
+  uint8_t* hsq_sf;
 };
+
+inline bool is_mx(int fmt) { return fmt == MOE_FMT_MXFP4 || fmt == MOE_FMT_MXFP8; }
+
+// bytes of n MX-coded elements (MXFP4 packs two per byte)
+inline size_t mx_code_bytes(int fmt, size_t n) { return fmt == MOE_FMT_MXFP4 ? n / 2 : n; }
+
+// MX layers: both operands in the same MX format, E8M0 scales, no global
+// scales; the reduction lengths meet the MX GEMMs' stage sizes.
+int validate_mx_layer(const moe_layer* L) {
+  if (L->act_fmt != L->w_fmt) return MOE_ERR_UNSUPPORTED;
+  const int kq = L->w_fmt == MOE_FMT_MXFP4 ? 512 : 256;
+  if (L->H % kq || L->I % kq || L->I_s % kq) return MOE_ERR_UNSUPPORTED;
+  if (!L->w13 || !L->w2 || !L->w13_sf || !L->w2_sf) return MOE_ERR_INVALID_ARG;
+  if (L->I_s && (!L->ws13 || !L->ws2 || !L->ws13_sf || !L->ws2_sf)) return MOE_ERR_INVALID_ARG;
+  if (L->ws_gate && (!L->I_s || !aligned(L->ws_gate, 16))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
 
 int validate_layer(const moe_layer* L) {
   if (!L) return MOE_ERR_INVALID_ARG;
   if (L->H < 1 || L->E < 1 || L->k < 1 || L->I < 1 || L->I_s < 0) return MOE_ERR_INVALID_ARG;
   if (L->k > L->E || L->k > 32 || L->E > 1024) return MOE_ERR_UNSUPPORTED;
   if (L->H % 64 || L->I % 64 || L->I_s % 64) return MOE_ERR_UNSUPPORTED;
+  if (is_mx(L->w_fmt) || is_mx(L->act_fmt)) return validate_mx_layer(L);
   const bool w4 = L->w_fmt == MOE_FMT_NVFP4, a4 = L->act_fmt == MOE_FMT_NVFP4;
   if (L->w_fmt != MOE_FMT_BF16 && !w4) return MOE_ERR_INVALID_ARG;
   if (L->act_fmt != MOE_FMT_BF16 && !a4) return MOE_ERR_INVALID_ARG;
@@ -77,7 +100,22 @@ size_t carve(const moe_layer* L, int T, void* ws, size_t cap, FwdBufs* b) {
   b->xp_sf = b->h_sf = b->hs_sf = nullptr;
   b->hs = nullptr;
   b->Ys = nullptr;
-  if (a4) {
+  b->hq = b->hq_sf = b->hsq = b->hsq_sf = nullptr;
+  if (is_mx(L->w_fmt)) {
+    const int f = L->w_fmt;
+    b->xq = c.take<uint8_t>(mx_code_bytes(f, static_cast<size_t>(T) * L->H));
+    b->xsf = c.take<uint8_t>(static_cast<size_t>(T) * L->H / 32);
+    b->xp = c.take<uint8_t>(mx_code_bytes(f, Tk * L->H));
+    b->xp_sf = c.take<uint8_t>(Tk * L->H / 32);
+    b->h = c.take<uint16_t>(Tk * L->I);
+    b->hq = c.take<uint8_t>(mx_code_bytes(f, Tk * L->I));
+    b->hq_sf = c.take<uint8_t>(Tk * L->I / 32);
+    if (L->I_s) {
+      b->hs = c.take<uint16_t>(static_cast<size_t>(T) * L->I_s);
+      b->hsq = c.take<uint8_t>(mx_code_bytes(f, static_cast<size_t>(T) * L->I_s));
+      b->hsq_sf = c.take<uint8_t>(static_cast<size_t>(T) * L->I_s / 32);
+    }
+  } else if (a4) {
     b->xq = c.take<uint8_t>(static_cast<size_t>(T) * L->H / 2);
     b->xsf = c.take<uint8_t>(static_cast<size_t>(T) * L->H / 16);
     b->gx = c.take<float>(1);
@@ -114,6 +152,8 @@ extern "C" size_t moe_forward_workspace_size(const moe_layer* L, int T) {
 }
 
 extern "C" int moe_route_ex(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
+                            void* stream);
+extern "C" int moe_quant_mx(const uint16_t* x, int rows, int cols, int fmt, uint8_t* codes, uint8_t* scales,
                             void* stream);
 
 namespace {
@@ -156,6 +196,30 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
   MOE_TRY(moe_route_ex(logits, T, E, k, L->no_renorm ? 0 : 1, b.idx, b.w, stream));
   if (b.gate) MOE_TRY(shared_gate_launch(x, L->ws_gate, T, H, b.gate, s));
   MOE_TRY(mark(events, 1, s));
+  if (is_mx(L->w_fmt)) {
+    // MX layers: x quantised in blocks of 32 along H; the GEMMs keep h in
+    // bf16, which is quantised the same way along I before the down
+    // projection (inside the gate/up window of the stage events)
+    const int f = L->w_fmt;
+    const int I = L->I, I_s = L->I_s;
+    MOE_TRY(moe_quant_mx(x, T, H, f, b.xq, b.xsf, stream));
+    MOE_TRY(mark(events, 2, s));
+    MOE_TRY(permute_launch(b.idx, T, k, E, b.xq, static_cast<int>(mx_code_bytes(f, H)), b.xsf, H / 32, b.counts,
+                           b.offsets, b.row_of, b.src_tok, b.xp, b.xp_sf, b.perm_ws, b.perm_ws_bytes, s));
+    MOE_TRY(mark(events, 3, s));
+    GemmProblem r1{b.xp, b.xp_sf, nullptr, Tk, L->w13, L->w13_sf, nullptr, E, b.h, nullptr, nullptr, I, H};
+    GemmProblem s1{b.xq, b.xsf, nullptr, T, L->ws13, L->ws13_sf, nullptr, 1, b.hs, nullptr, nullptr, I_s, H};
+    MOE_TRY(grouped_gemm_launch(MOE_EPI_SWIGLU_BF16, f, f, r1, b.offsets, E, I_s ? &s1 : nullptr, T, s));
+    MOE_TRY(moe_quant_mx(static_cast<const uint16_t*>(b.h), Tk, I, f, b.hq, b.hq_sf, stream));
+    if (I_s) MOE_TRY(moe_quant_mx(static_cast<const uint16_t*>(b.hs), T, I_s, f, b.hsq, b.hsq_sf, stream));
+    MOE_TRY(mark(events, 4, s));
+    GemmProblem r2{b.hq, b.hq_sf, nullptr, Tk, L->w2, L->w2_sf, nullptr, E, b.Y, nullptr, nullptr, H, I};
+    GemmProblem s2{b.hsq, b.hsq_sf, nullptr, T, L->ws2, L->ws2_sf, nullptr, 1, b.Ys, nullptr, nullptr, H, I_s};
+    MOE_TRY(grouped_gemm_launch(MOE_EPI_STORE_BF16, f, f, r2, b.offsets, E, I_s ? &s2 : nullptr, T, s));
+    MOE_TRY(mark(events, 5, s));
+    MOE_TRY(combine_launch(b.Y, b.row_of, b.w, b.Ys, b.gate, T, k, H, out, s));
+    return mark(events, 6, s);
+  }
   if (a4) MOE_TRY(quant_launch(x, 1, T, H, nullptr, b.xq, b.xsf, b.gx, b.qws, quant_ws_bytes(1), s));
   MOE_TRY(mark(events, 2, s));
   // NVFP4 weights with bf16 activations: when the tensor-memory kernel takes

@@ -12,9 +12,9 @@ from typing import Optional
 import torch
 
 from . import api
-from ._lib import MOE_FMT_BF16, MOE_FMT_NVFP4, MoeLayerC
+from ._lib import MOE_FMT_BF16, MOE_FMT_MXFP4, MOE_FMT_MXFP8, MOE_FMT_NVFP4, MoeLayerC
 
-_FMT = {"bf16": MOE_FMT_BF16, "nvfp4": MOE_FMT_NVFP4}
+_FMT = {"bf16": MOE_FMT_BF16, "nvfp4": MOE_FMT_NVFP4, "mxfp8": MOE_FMT_MXFP8, "mxfp4": MOE_FMT_MXFP4}
 
 
 @dataclass
@@ -29,6 +29,19 @@ def quantize_weights(w: torch.Tensor) -> NVFP4Tensor:
     scale per group."""
     codes, sf, g = api.moe_quant_nvfp4(w.contiguous())
     return NVFP4Tensor(codes, sf, g)
+
+
+@dataclass
+class MXTensor:
+    codes: torch.Tensor  # uint8 [..., cols] (MXFP8) or [..., cols/2] (MXFP4)
+    sf: torch.Tensor     # uint8 [..., cols/32] (E8M0)
+
+
+def quantize_weights_mx(w: torch.Tensor, fmt: str) -> MXTensor:
+    """bf16 [..., rows, cols] -> MXFP8 / MXFP4 along cols (moe_quant_mx)."""
+    w = w.contiguous()
+    codes, sf = api.moe_quant_mx(w.reshape(-1, w.shape[-1]), _FMT[fmt])
+    return MXTensor(codes.reshape(w.shape[:-1] + (codes.shape[-1],)), sf.reshape(w.shape[:-1] + (sf.shape[-1],)))
 
 
 def _check_weight(t: Optional[torch.Tensor], name: str, shape, device=None) -> None:
@@ -69,7 +82,21 @@ class MoELayer:
         c = MoeLayerC()
         c.H, c.E, c.k, c.I, c.I_s = H, E, k, I, I_s
         c.w_fmt, c.act_fmt = _FMT[w_fmt], _FMT[act_fmt]
-        if w_fmt == "bf16":
+        if w_fmt.startswith("mx"):
+            if act_fmt != w_fmt:
+                raise ValueError("MX layers take the same MX format for weights and activations")
+            self.w13 = quantize_weights_mx(w13, w_fmt)
+            self.w2 = quantize_weights_mx(w2, w_fmt)
+            c.w13, c.w13_sf = self.w13.codes.data_ptr(), self.w13.sf.data_ptr()
+            c.w2, c.w2_sf = self.w2.codes.data_ptr(), self.w2.sf.data_ptr()
+            self._keep += [self.w13, self.w2]
+            if I_s:
+                self.ws13 = quantize_weights_mx(ws13, w_fmt)
+                self.ws2 = quantize_weights_mx(ws2, w_fmt)
+                c.ws13, c.ws13_sf = self.ws13.codes.data_ptr(), self.ws13.sf.data_ptr()
+                c.ws2, c.ws2_sf = self.ws2.codes.data_ptr(), self.ws2.sf.data_ptr()
+                self._keep += [self.ws13, self.ws2]
+        elif w_fmt == "bf16":
             self.w13, self.w2 = w13.contiguous(), w2.contiguous()
             c.w13, c.w2 = self.w13.data_ptr(), self.w2.data_ptr()
             self._keep += [self.w13, self.w2]
@@ -89,7 +116,7 @@ class MoELayer:
                 c.ws13, c.ws13_sf, c.ws13_g = (t.data_ptr() for t in (self.ws13.codes, self.ws13.sf, self.ws13.g))
                 c.ws2, c.ws2_sf, c.ws2_g = (t.data_ptr() for t in (self.ws2.codes, self.ws2.sf, self.ws2.g))
                 self._keep += [self.ws13, self.ws2]
-        if act_fmt == "nvfp4":
+        if act_fmt == "nvfp4" and w_fmt == "nvfp4":
             self.g_h = torch.tensor([g_h], dtype=torch.float32, device=self.device)
             self.g_hs = torch.tensor([g_h if g_hs is None else g_hs], dtype=torch.float32, device=self.device)
             c.g_h, c.g_hs = self.g_h.data_ptr(), self.g_hs.data_ptr()

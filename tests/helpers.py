@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from oracle import nvfp4
+from oracle import mx, nvfp4
 
 F32 = np.float32
 
@@ -39,6 +39,9 @@ class OracleWeights:
         a = to_np_f32(w)
         if self.cfg.w_fmt == "bf16":
             return a.astype(np.float64), None
+        if self.cfg.w_fmt.startswith("mx"):
+            q, s = mx.quantize(a, self.cfg.w_fmt)
+            return mx.dequantize(q, s, self.cfg.w_fmt), (q, s)
         q, s, g = nvfp4.quantize(a)
         return nvfp4.dequantize(q, s, g), (q, s, g)
 
@@ -69,14 +72,19 @@ def oracle_layer(cfg: synth.LayerConfig, acts: synth.Activations, ow: OracleWeig
     renorm / shared_g select the router and shared-gate variants (the gate sees
     the bf16 activations)."""
     x = to_np_f32(acts.x)
+    hq = None
     if cfg.act_fmt == "nvfp4":
         q, s, g = nvfp4.quantize(x)  # one global scale over the whole input
         x_deq = nvfp4.dequantize(q, s, g)
         gh = F32(cfg.g_h)
+    elif cfg.act_fmt.startswith("mx"):
+        x_deq = mx.fake_quant(x, cfg.act_fmt)  # blocks of 32 along H, no global scale
+        gh = None
+        hq = mx.h_quant(cfg.act_fmt)
     else:
         x_deq = x.astype(np.float64)
         gh = None
     return oracle.forward(x_deq, acts.logits.numpy(), cfg.k, cfg.E, ow.expert, ow.shared(), tokens=tokens,
-                          h_quant_g=gh, hs_quant_g=gh, renorm=renorm,
+                          h_quant_g=gh, hs_quant_g=gh, renorm=renorm, h_quant=hq, hs_quant=hq,
                           shared_g=None if shared_g is None else to_np_f32(shared_g).astype(np.float64),
                           x_gate=x.astype(np.float64))

@@ -1,0 +1,54 @@
+"""MX layers (MXFP8 and MXFP4 weights and activations) through moe_forward
+against the fp64 oracle on every token: x quantised in blocks of 32 along
+H, h rounded to bf16 and quantised the same way along I, weights encoded by
+the oracle's own MX codec from the bf16 masters.  Tolerance 1e-2 relative
+Frobenius (as for the NVFP4 layers).
+
+The MX kernels have not run on a GPU yet, so the module runs only when
+MOE_RUN_UNVALIDATED=1 is set."""
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.helpers import OracleWeights, oracle_layer, require_gpu, to_np_f32
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(os.environ.get("MOE_RUN_UNVALIDATED") != "1",
+                                 reason="MX layers not yet run on a GPU; opt in with MOE_RUN_UNVALIDATED=1")]
+DEV = "cuda"
+
+
+def mx_layer(fmt):
+    """Small MX layers: Qwen3-235B-like (no shared expert) in MXFP8, the
+    format the pages serve it in, and DeepSeek-V3-like (shared expert) in
+    MXFP4."""
+    if fmt == "mxfp8":
+        base = synth.small_variant(synth.QWEN3_235B, H=512, E=16, k=4, I=256, name="qwen3-mxfp8-small")
+    else:
+        base = synth.small_variant(synth.DEEPSEEK_V3, H=512, E=16, k=4, I=512, I_s=512, name="ds-mxfp4-small")
+    return dataclasses.replace(base, w_fmt=fmt, act_fmt=fmt)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("T", [1, 37, 300])
+def test_mx_layer_all_tokens(fmt, T):
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
+    cfg = mx_layer(fmt)
+    acts = synth.make_activations(cfg, T, seed=T)
+    w = synth.make_weights(cfg, seed=0, device=DEV)
+    layer = MoELayer.from_config(cfg, w)
+    out = layer(acts.x.to(DEV), acts.logits.to(DEV))
+    assert moe_sync_status() == 0
+    got = to_np_f32(out)
+    ref, *_ = oracle_layer(cfg, acts, OracleWeights(cfg, w))
+    err = oracle.rel_frobenius(got, ref)
+    assert err <= 1e-2, err
