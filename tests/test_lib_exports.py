@@ -134,3 +134,21 @@ def test_mxfp4_grouped_gemm_checks_arguments_on_the_host(lib):
     assert gemm(M8, MX, 0, 512) == L.MOE_ERR_UNSUPPORTED
     assert gemm(M8, M8, 0, 320) == L.MOE_ERR_UNSUPPORTED     # K % 256 != 0
     assert gemm(M8, M8, 0, 256, sf=P(260)) == L.MOE_ERR_INVALID_ARG  # scales not 8-byte aligned
+
+
+def test_mx_layer_validation(lib):
+    from mixture_experts_layer_fwd_gb300 import _lib as L
+    c = L.MoeLayerC()
+    c.H, c.E, c.k, c.I, c.I_s = 512, 8, 2, 512, 0
+    c.w_fmt = c.act_fmt = L.MOE_FMT_MXFP4
+    c.w13, c.w2, c.w13_sf, c.w2_sf = 4096, 8192, 12288, 16384
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), 64) > 0
+    c.act_fmt = L.MOE_FMT_MXFP8  # weights and activations in the same MX format
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), 64) == 0
+    c.act_fmt = L.MOE_FMT_MXFP4
+    c.I = 256  # MXFP4 needs multiples of 512
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), 64) == 0
+    c.w_fmt = c.act_fmt = L.MOE_FMT_MXFP8  # MXFP8: multiples of 256
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), 64) > 0
+    c.w2_sf = None
+    assert lib.moe_forward_workspace_size(ctypes.byref(c), 64) == 0
