@@ -32,6 +32,10 @@
  *    e2m1(q) * e4m3(s) * g ("Driving vLLM WideEP and Large-Scale Serving
  *    Toward Maturity on Blackwell (Part I)", sections "NVFP4 GEMM for MoE and
  *    O-proj" and "NVFP4 MoE dispatch").
+ *  - MX tensors (MOE_FMT_MXFP8 / MOE_FMT_MXFP4) are codes (E4M3 bytes, or
+ *    E2M1 packed as for NVFP4) and one E8M0 scale byte per 32 consecutive
+ *    elements along the reduction dimension ([rows, cols/32]); no global
+ *    scale.  Decoded value = element(q) * 2^(s - 127) (moe_quant_mx).
  *  - Argument errors are detected on the host before anything is launched:
  *    MOE_ERR_INVALID_ARG (null or misaligned pointer, negative size),
  *    MOE_ERR_UNSUPPORTED (shape outside what the kernels handle, see each
@@ -41,6 +45,10 @@
  *    Each is bounded in time (moe_set_wait_timeout_ns, default 1 s); a wait
  *    that runs out records MOE_ERR_TIMEOUT in a device error word and the
  *    kernel returns.  moe_sync_status() reports (and clears) it.
+ *  - What only the device reads is checked there, so that no input sends a
+ *    kernel outside its buffers: expert ids outside [0, E) (left out of the
+ *    permutation, reported as MOE_ERR_INVALID_ARG by moe_sync_status()),
+ *    combine rows outside [0, T*k) (skipped), group offsets (clamped).
  *  - The first call on each device that launches a permutation or a grouped
  *    GEMM looks up the device error word (cudaGetSymbolAddress) and sets
  *    kernel attributes; make such a call once before capturing any of them
