@@ -148,23 +148,30 @@ def moe_permute_noalloc(idx: torch.Tensor, E: int, x_rows: Optional[torch.Tensor
     T, k = idx.shape
     dev = idx.device
     o = dict(out or {})
-    o.setdefault("counts", torch.empty(E, dtype=torch.int32, device=dev))
-    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
-    o.setdefault("row_of", torch.empty(T, k, dtype=torch.int32, device=dev))
-    o.setdefault("src_tok", torch.empty(T * k, dtype=torch.int32, device=dev))
+
+    def need(key, make):
+        # allocate only what the caller did not pass (a setdefault would build
+        # the default tensor, and so allocate, even when the key is present)
+        if o.get(key) is None:
+            o[key] = make()
+
+    need("counts", lambda: torch.empty(E, dtype=torch.int32, device=dev))
+    need("offsets", lambda: torch.empty(E + 1, dtype=torch.int32, device=dev))
+    need("row_of", lambda: torch.empty(T, k, dtype=torch.int32, device=dev))
+    need("src_tok", lambda: torch.empty(T * k, dtype=torch.int32, device=dev))
     row_bytes = sf_bytes = 0
     if x_rows is not None:
         _dev(x_rows, "x_rows", device=dev)
         if x_rows.shape[0] != T:
             raise ValueError("x_rows: expected one row per token")
         row_bytes = x_rows[0].numel() * x_rows.element_size() if T else 0
-        o.setdefault("xp", torch.empty((T * k,) + tuple(x_rows.shape[1:]), dtype=x_rows.dtype, device=dev))
+        need("xp", lambda: torch.empty((T * k,) + tuple(x_rows.shape[1:]), dtype=x_rows.dtype, device=dev))
         if x_sf is not None:
             _dev(x_sf, "x_sf", dtype=torch.uint8, device=dev)
             if x_sf.dim() != 2 or x_sf.shape[0] != T:
                 raise ValueError("x_sf: expected [T, sf_bytes]")
             sf_bytes = x_sf.shape[1]
-            o.setdefault("xp_sf", torch.empty(T * k, sf_bytes, dtype=torch.uint8, device=dev))
+            need("xp_sf", lambda: torch.empty(T * k, sf_bytes, dtype=torch.uint8, device=dev))
     o.setdefault("xp", None)
     o.setdefault("xp_sf", None)
     # caller-given outputs are written by the kernels: check them like inputs

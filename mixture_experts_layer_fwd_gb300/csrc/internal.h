@@ -5,6 +5,8 @@
 
 namespace moe {
 
+constexpr int kPermChunk = 1024;        // routed slots per chunk of the permutation
+constexpr int kPermMaxExperts = 4096;   // largest E the permutation takes (E int32 of shared memory)
 size_t permute_ws_bytes(int T, int k, int E);
 // to_f16: the rows are bf16 and are written to xp_rows as fp16 (saturating).
 int permute_launch(const int32_t* idx, int T, int k, int E, const void* x_rows, int row_bytes, const uint8_t* x_sf,

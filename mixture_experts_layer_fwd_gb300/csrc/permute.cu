@@ -27,8 +27,6 @@
 
 namespace moe {
 
-constexpr int kPermChunk = 1024;   // slots per chunk
-constexpr int kMaxExperts = 4096;
 
 __global__ void __launch_bounds__(256) permute_count_kernel(const int32_t* __restrict__ idx, int S, int E,
                                                             int32_t* __restrict__ hist, unsigned int* err) {
@@ -246,7 +244,7 @@ extern "C" int moe_permute(const int32_t* idx, int T, int k, int E, const void* 
                            int32_t* row_of, int32_t* src_tok, void* xp_rows, uint8_t* xp_sf, void* ws,
                            size_t ws_bytes, void* stream) {
   if (T < 0 || k < 1 || E < 1) return MOE_ERR_INVALID_ARG;
-  if (E > kMaxExperts || k > E) return MOE_ERR_UNSUPPORTED;
+  if (E > kPermMaxExperts || k > E) return MOE_ERR_UNSUPPORTED;
   // the row copy runs one warp per routed row (32 * T*k threads in 32 bits)
   if (static_cast<long long>(T) * k >= (1ll << 27)) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;

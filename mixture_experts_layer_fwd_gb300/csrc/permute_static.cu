@@ -19,32 +19,37 @@
 // ordering) race on it; calls ordered on one stream are safe.  Nothing in the
 // array needs clearing between calls: the kernels write every entry they later
 // read.
+#include <atomic>
+
 #include "internal.h"
 
 namespace moe {
 namespace {
 
 constexpr size_t kStaticEntries = 131072;  // int32 entries per scratch array
-constexpr int kChunk = 1024;               // slots per chunk (as in permute.cu)
 
 static __device__ __align__(256) int32_t g_permute_scratch[2 * kStaticEntries];
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the array's name in host code is only a stand-in).
+// per device (the array's name in host code is only a stand-in).  Host
+// threads may make their first calls at the same time: the entries are
+// atomics, and a racing lookup stores the same address.
 int32_t* static_scratch() {
-  static int32_t* cache[64] = {nullptr};
+  static std::atomic<int32_t*> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (cache[dev] == nullptr) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+  int32_t* p = cache[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void* a = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_permute_scratch);
     if (e != cudaSuccess) {
       set_cuda_error(e);
       return nullptr;
     }
-    cache[dev] = static_cast<int32_t*>(p);
+    p = static_cast<int32_t*>(a);
+    cache[dev].store(p, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return p;
 }
 
 }  // namespace
@@ -56,10 +61,12 @@ extern "C" int moe_permute_noalloc(const int32_t* idx, int T, int k, int E, cons
                                    const uint8_t* x_sf, int sf_row_bytes, int32_t* counts, int32_t* offsets,
                                    int32_t* row_of, int32_t* src_tok, void* xp_rows, uint8_t* xp_sf,
                                    void* stream) {
+  // the same size checks as moe_permute, then the scratch limit
   if (T < 0 || k < 1 || E < 1) return MOE_ERR_INVALID_ARG;
-  if (k > E) return MOE_ERR_UNSUPPORTED;
+  if (E > kPermMaxExperts || k > E) return MOE_ERR_UNSUPPORTED;
   const long long slots = static_cast<long long>(T) * k;
-  const long long chunks = (slots + kChunk - 1) / kChunk;
+  if (slots >= (1ll << 27)) return MOE_ERR_UNSUPPORTED;
+  const long long chunks = (slots + kPermChunk - 1) / kPermChunk;
   if (chunks * E > static_cast<long long>(kStaticEntries)) return MOE_ERR_UNSUPPORTED;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!idx || !row_of || !src_tok)) return MOE_ERR_INVALID_ARG;

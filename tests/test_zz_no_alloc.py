@@ -41,6 +41,12 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     # the largest sizes inside the limit pass the size check (then fail on the null outputs)
     assert call(16384, 8, 1024) == L.MOE_ERR_INVALID_ARG
     assert call(4096, 8, 4096) == L.MOE_ERR_INVALID_ARG
+    # moe_permute's own limits hold here too: E <= 4096 (its shared-memory
+    # histogram), even where the scratch would hold the problem
+    for E in (4097, 8192, 16384):
+        assert call(1, 1, E) == L.MOE_ERR_UNSUPPORTED, E
+        assert lib.moe_permute(None, 1, 1, E, None, 0, None, 0, None, None, None, None, None, None, None, 0,
+                               None) == L.MOE_ERR_UNSUPPORTED
 
 
 def _routing(T, E, k, seed):
@@ -85,3 +91,33 @@ def test_noalloc_permute_matches_moe_permute_on_two_calls():
         # and the permutation is the oracle's
         p = oracle.permute(idx.cpu().numpy(), E)
         assert np.array_equal(got["src_tok"].cpu().numpy(), p.src_tok)
+
+
+@pytest.mark.gpu
+def test_noalloc_binding_with_all_outputs_allocates_nothing():
+    """Through the Python binding with every output passed in, the call makes
+    no device allocation (the caching allocator's count stays put)."""
+    require_gpu()
+    from mixture_experts_layer_fwd_gb300 import moe_permute, moe_permute_noalloc
+    T, E, k, H = 777, 64, 4, 1024
+    idx = _routing(T, E, k, seed=5).to(DEV)
+    rows = torch.randint(0, 256, (T, H // 2), generator=torch.Generator().manual_seed(1),
+                         dtype=torch.uint8).to(DEV)
+    sf = torch.randint(0, 256, (T, H // 16), generator=torch.Generator().manual_seed(2),
+                       dtype=torch.uint8).to(DEV)
+    out = dict(counts=torch.empty(E, dtype=torch.int32, device=DEV),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV),
+               row_of=torch.empty(T, k, dtype=torch.int32, device=DEV),
+               src_tok=torch.empty(T * k, dtype=torch.int32, device=DEV),
+               xp=torch.empty(T * k, H // 2, dtype=torch.uint8, device=DEV),
+               xp_sf=torch.empty(T * k, H // 16, dtype=torch.uint8, device=DEV))
+    moe_permute_noalloc(idx, E, rows, sf, out=out)  # first call: looks up the scratch address
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_stats()["allocation.all.allocated"]
+    got = moe_permute_noalloc(idx, E, rows, sf, out=out)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_stats()["allocation.all.allocated"] == before
+    ref = moe_permute(idx, E, rows, sf)
+    for key in ("counts", "offsets", "row_of", "src_tok", "xp", "xp_sf"):
+        assert got[key] is out[key]
+        assert torch.equal(got[key], ref[key]), key
