@@ -16,9 +16,13 @@
  * --------------------------------
  *  - Every call returns an int status (MOE_OK or one of MOE_ERR_*).
  *  - All tensors are caller-owned DEVICE pointers unless a parameter says
- *    "host".  The library never allocates or frees memory: scratch space is a
- *    caller-supplied workspace whose size the matching *_workspace_size()
- *    call returns.  Workspaces must be 256-byte aligned.
+ *    "host".  The compute calls never allocate or free memory: scratch space
+ *    is a caller-supplied workspace whose size the matching
+ *    *_workspace_size() call returns.  Workspaces must be 256-byte aligned.
+ *    The exceptions are named where they are declared: the CUDA-graph calls
+ *    (moe_forward_graph_create creates a stream and an executable graph,
+ *    moe_graph_destroy frees the graph) and the fixed device array of
+ *    moe_permute_noalloc.
  *  - Every call is asynchronous on the caller's CUDA stream (`stream` is a
  *    cudaStream_t passed as void*; NULL is the legacy default stream).  The
  *    library does no host synchronisation except in moe_sync_status() and
@@ -234,7 +238,8 @@ int moe_quant_nvfp4(const uint16_t* x, int groups, int rows, int cols,
  *            [rows, cols/2] (element 2j in the low nibble; 4-byte aligned)
  *   scales : uint8 [rows, cols/32]
  * cols must be a multiple of 32.  No workspace, no tensor-wide scale.
- * Not yet validated on hardware. */
+ * x must be finite: a block holding Inf or NaN gets an unspecified scale
+ * and codes. */
 int moe_quant_mx(const uint16_t* x, int rows, int cols, int fmt, uint8_t* codes, uint8_t* scales,
                  void* stream);
 
@@ -251,7 +256,7 @@ int moe_quant_mx(const uint16_t* x, int rows, int cols, int fmt, uint8_t* codes,
  * [G, Wn, K/16], W_g [G]); Wn = N (STORE) or 2N (SWIGLU).  Scale pointers
  * (A_g, W_g, c_g) are device pointers; pass NULL for bf16 operands.
  * SWIGLU_NVFP4 writes C = codes [M_total, N/2] and C_sf [M_total, N/16].
- * MX formats (a_fmt = w_fmt; not yet validated on hardware), scales E8M0
+ * MX formats (a_fmt = w_fmt), scales E8M0
  * [.., K/32] (moe_quant_mx), no global scales (A_g, W_g, c_g ignored),
  * STORE_BF16 and SWIGLU_BF16 only:
  *   MOE_FMT_MXFP4: codes as NVFP4; K % 512 == 0, 16-byte aligned scales
@@ -317,8 +322,17 @@ int moe_shared_gate(const uint16_t* x, const uint16_t* g, int T, int H,
  *                  scale over x) before dispatch, and the SwiGLU output h is
  *                  quantised to NVFP4 with the caller's global scales
  *                  *g_h (routed) and *g_hs (shared) before the down GEMM.
- *   MX layers (w_fmt = act_fmt = MOE_FMT_MXFP4 or MOE_FMT_MXFP8; not yet
- *                  validated on hardware): codes as moe_quant_mx writes them
+ *   NVFP4 weights with bf16 activations: when H, I and I_s are multiples
+ *                  of 256 and the weight scales 16-byte aligned, the layer
+ *                  runs its fp16 tensor-core path: x is converted to fp16
+ *                  while it is permuted and h is kept in fp16.  bf16 -> fp16
+ *                  is exact for 2^-14 <= |x| <= 65504; larger magnitudes
+ *                  saturate to +-65504 and magnitudes below 2^-14 keep fewer
+ *                  significant bits (fp16 subnormals), so activations or h
+ *                  outside that range give results that differ from a bf16
+ *                  computation.  Other shapes compute in bf16.
+ *   MX layers (w_fmt = act_fmt = MOE_FMT_MXFP4 or MOE_FMT_MXFP8): codes
+ *                  as moe_quant_mx writes them
  *                  (w13 [E, 2I, H or H/2], w2 [E, H, I or I/2]), scales E8M0
  *                  [.., K/32], no global scales (*_g, g_h, g_hs ignored); x
  *                  and h are quantised the same way inside the layer, h from

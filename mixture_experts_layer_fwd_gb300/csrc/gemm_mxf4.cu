@@ -1,7 +1,7 @@
 // Grouped GEMM with both operands in MXFP4: E2M1 codes with one E8M0 scale
 // per 32 elements along K, on the block-scaled FP4 tensor cores
 // (tcgen05.mma kind::mxf4nvf4, block_scale, scale_vec::2X), 512-element k
-// stages.  Not yet validated on hardware.
+// stages.
 //
 // "Hosting Qwen on Blackwell", section "Quantização": Blackwell runs the
 // microscaled formats natively, Qwen3-235B is served in MXFP8 and MXFP4 was

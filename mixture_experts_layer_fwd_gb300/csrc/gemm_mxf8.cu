@@ -1,7 +1,6 @@
 // Grouped GEMM with both operands in MXFP8: E4M3 bytes with one E8M0 scale
 // per 32 elements along K, on the block-scaled tensor cores (tcgen05.mma
-// kind::mxf8f6f4, block_scale, scale_vec::1X).  Not yet validated on
-// hardware.
+// kind::mxf8f6f4, block_scale, scale_vec::1X).
 //
 // "Hosting Qwen on Blackwell", section "Quantização": Qwen3-235B is served
 // with its weights converted to MXFP8 once after fine-tuning, which ran much

@@ -2,11 +2,7 @@
 MOE_FMT_MXFP4 / MOE_FMT_MXFP8) against the fp64 product of the oracle's
 dequantised operands (oracle/mx.py): ragged and empty groups, both bf16
 epilogues, a one-group one-stage case first (the smallest check of the
-block-scale descriptor and byte selection).
-
-The kernels have not run on a GPU yet, so the module runs only when
-MOE_RUN_UNVALIDATED=1 is set."""
-import os
+block-scale descriptor and byte selection)."""
 
 import numpy as np
 import pytest
@@ -16,9 +12,7 @@ import oracle
 from oracle import mx
 from tests.helpers import require_gpu
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skipif(os.environ.get("MOE_RUN_UNVALIDATED") != "1",
-                                 reason="MXFP4 GEMM not yet run on a GPU; opt in with MOE_RUN_UNVALIDATED=1")]
+pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 FMT = {"mxfp8": 2, "mxfp4": 3}

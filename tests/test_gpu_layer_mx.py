@@ -2,12 +2,8 @@
 against the fp64 oracle on every token: x quantised in blocks of 32 along
 H, h rounded to bf16 and quantised the same way along I, weights encoded by
 the oracle's own MX codec from the bf16 masters.  Tolerance 1e-2 relative
-Frobenius (as for the NVFP4 layers).
-
-The MX kernels have not run on a GPU yet, so the module runs only when
-MOE_RUN_UNVALIDATED=1 is set."""
+Frobenius (as for the NVFP4 layers)."""
 import dataclasses
-import os
 
 import numpy as np
 import pytest
@@ -16,9 +12,7 @@ import oracle
 import synth
 from tests.helpers import OracleWeights, oracle_layer, require_gpu, to_np_f32
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skipif(os.environ.get("MOE_RUN_UNVALIDATED") != "1",
-                                 reason="MX layers not yet run on a GPU; opt in with MOE_RUN_UNVALIDATED=1")]
+pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 

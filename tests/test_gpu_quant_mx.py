@@ -4,11 +4,7 @@
 Inputs: normal rows with x20 outliers, all-zero blocks, blocks of tiny
 values (subnormal abs-max), negative zeros, signed ties of both element
 grids times powers of two, and shapes from one 32-element block to the
-7168-wide deepseek-v3 rows (a partial last 256-column chunk included).
-
-The kernel has not run on a GPU yet, so the module runs only when
-MOE_RUN_UNVALIDATED=1 is set."""
-import os
+7168-wide deepseek-v3 rows (a partial last 256-column chunk included)."""
 
 import numpy as np
 import pytest
@@ -17,9 +13,7 @@ import torch
 from oracle import mx, nvfp4
 from tests.helpers import require_gpu
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skipif(os.environ.get("MOE_RUN_UNVALIDATED") != "1",
-                                 reason="MX quantiser not yet run on a GPU; opt in with MOE_RUN_UNVALIDATED=1")]
+pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 FMTS = {"mxfp8": 2, "mxfp4": 3}
