@@ -203,7 +203,10 @@ def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
               or the NVFP4-dequantised values on the NVFP4-activation path)
     logits  : fp32 [T, E] router logits
     get_expert(e) -> ExpertWeights, called once per expert that the selected
-              tokens use (lets the caller decode weights lazily)
+              tokens use (lets the caller decode weights lazily); None stands
+              for an expert whose weights are all zero: its gate, up, h and
+              output are then exactly zero (zero also stays zero through the
+              h quantisers: it encodes to code 0), so its rows add nothing
     Returns (out fp64 [len(tokens), H], idx, w, perm) where idx / w / perm
     cover the full T (routing is cheap) and out covers `tokens`.
     renorm  : False selects the router without renormalisation (see route)
@@ -227,6 +230,8 @@ def forward(x_deq: np.ndarray, logits: np.ndarray, k: int, E: int,
         if not rows:
             continue
         W = get_expert(e)
+        if W is None:
+            continue
         src = perm.src_tok[rows]
         y = expert_mlp(x_deq[src], W.w13, W.w2, h_quant_g, h_quant)
         for r, t, yr in zip(rows, src, y):

@@ -31,9 +31,17 @@ class OracleWeights:
     the oracle's own NVFP4 quantiser on the NVFP4 workloads (one global scale
     per expert and projection, like the CUDA path's weight preparation)."""
 
-    def __init__(self, cfg: synth.LayerConfig, master: synth.MasterWeights):
+    def __init__(self, cfg: synth.LayerConfig, master: synth.MasterWeights, cache: bool = True,
+                 zero_experts=()):
+        """cache=False decodes each expert when asked and keeps nothing (host
+        memory stays at one expert on the full-size workloads).
+        zero_experts: experts whose master weights the caller has set to
+        zero; the oracle skips them (expert() returns None, see
+        oracle.forward)."""
         self.cfg, self.m = cfg, master
         self.cache = {}
+        self.keep = cache
+        self.zero = set(int(e) for e in zero_experts)
 
     def _decode(self, w: torch.Tensor):
         a = to_np_f32(w)
@@ -45,12 +53,17 @@ class OracleWeights:
         q, s, g = nvfp4.quantize(a)
         return nvfp4.dequantize(q, s, g), (q, s, g)
 
-    def expert(self, e: int) -> oracle.ExpertWeights:
-        if e not in self.cache:
-            w13, _ = self._decode(self.m.w13[e])
-            w2, _ = self._decode(self.m.w2[e])
-            self.cache[e] = oracle.ExpertWeights(w13, w2)
-        return self.cache[e]
+    def expert(self, e: int):
+        if e in self.zero:
+            return None
+        if e in self.cache:
+            return self.cache[e]
+        w13, _ = self._decode(self.m.w13[e])
+        w2, _ = self._decode(self.m.w2[e])
+        ew = oracle.ExpertWeights(w13, w2)
+        if self.keep:
+            self.cache[e] = ew
+        return ew
 
     def expert_codes(self, e: int):
         """Oracle NVFP4 encoding of expert e: ((q13, s13, g13), (q2, s2, g2))."""
@@ -74,8 +87,15 @@ def oracle_layer(cfg: synth.LayerConfig, acts: synth.Activations, ow: OracleWeig
     x = to_np_f32(acts.x)
     hq = None
     if cfg.act_fmt == "nvfp4":
-        q, s, g = nvfp4.quantize(x)  # one global scale over the whole input
-        x_deq = nvfp4.dequantize(q, s, g)
+        # one global scale over the whole input; every row is then quantised
+        # on its own (blocks of 16 inside the row), so only the rows of the
+        # requested tokens are encoded (the others are never read)
+        g = nvfp4.global_scale(x)
+        rows = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
+        x_deq = np.zeros(x.shape, np.float64)
+        if len(rows):
+            q, s, _ = nvfp4.quantize(x[rows], g)
+            x_deq[rows] = nvfp4.dequantize(q, s, g)
         gh = F32(cfg.g_h)
     elif cfg.act_fmt.startswith("mx"):
         x_deq = mx.fake_quant(x, cfg.act_fmt)  # blocks of 32 along H, no global scale

@@ -294,6 +294,33 @@ def test_nvfp4_weights_on_grid_equal_bf16_path():
     np.testing.assert_array_equal(plain, quant)
 
 
+def test_zero_expert_as_none_equals_explicit_zero_weights():
+    """get_expert returning None (an expert whose weights are all zero) gives
+    the same layer as passing that expert's zero weights explicitly, also on
+    the NVFP4 h path: the NVFP4 and MX codecs take an all-zero matrix to
+    exactly zero."""
+    from oracle import mx
+    rng = np.random.default_rng(21)
+    T, H, E, k, I, I_s = 30, 32, 6, 2, 32, 32
+    experts, shared, x, logits = _tiny_layer(rng, T, H, E, k, I, I_s)
+    zero = {1, 4}
+    z = ExpertWeights(np.zeros((2 * I, H)), np.zeros((H, I)))
+    explicit, *_ = forward(x, logits, k, E, lambda e: z if e in zero else experts[e], shared,
+                           h_quant_g=F32(0.01))
+    skipped, *_ = forward(x, logits, k, E, lambda e: None if e in zero else experts[e], shared,
+                          h_quant_g=F32(0.01))
+    np.testing.assert_array_equal(explicit, skipped)
+    # the zero experts were routed to, so the test skipped real work
+    _, idx, *_ = forward(x, logits, k, E, lambda e: experts[e])
+    assert zero & set(idx.reshape(-1).tolist())
+    # all-zero weights quantise and decode to exact zeros in every format
+    zm = np.zeros((2 * I, H), np.float32)
+    p, sc, g = nvfp4.quantize(zm)
+    assert not nvfp4.dequantize(p, sc, g).any()
+    for fmt in ("mxfp8", "mxfp4"):
+        assert not mx.fake_quant(zm, fmt).any()
+
+
 def test_dropped_shared_or_weight_is_detected():
     """Plausible mistakes (shared expert dropped, weights not applied) move
     the output far beyond any tolerance used by the parity tests."""
