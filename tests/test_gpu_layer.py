@@ -2,9 +2,11 @@
 
 Tolerance (relative Frobenius error of the bf16 output): 5e-3 on the bf16
 weight path, 1e-2 on the NVFP4 paths.  Small shapes are compared on every
-token; the full-size workloads on a seeded token subsample (each output row
-depends only on its own token and the global activation scale, so the
-oracle evaluates those rows exactly)."""
+token.  The full-size workloads are compared on token subsets (each output
+row depends only on its own token and the global activation scale, so the
+oracle evaluates those rows exactly): a seeded sample with real weights on
+every expert, and every row of a few chosen experts with the other experts'
+weights set to zero."""
 import numpy as np
 import pytest
 import torch
@@ -27,7 +29,7 @@ def _tol(cfg):
     return 5e-3 if cfg.w_fmt == "bf16" else 1e-2
 
 
-def _run(cfg, T, seed=0, tokens=None, weights=None):
+def _run(cfg, T, seed=0, tokens=None, weights=None, cache=True):
     from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
     acts = synth.make_activations(cfg, T, seed=seed)
     w = weights or synth.make_weights(cfg, seed=seed, device=DEV)
@@ -36,7 +38,7 @@ def _run(cfg, T, seed=0, tokens=None, weights=None):
     assert moe_sync_status() == 0
     got = to_np_f32(out)
     assert np.isfinite(got).all()
-    ref, *_ = oracle_layer(cfg, acts, OracleWeights(cfg, w), tokens=tokens)
+    ref, *_ = oracle_layer(cfg, acts, OracleWeights(cfg, w, cache=cache), tokens=tokens)
     sel = got if tokens is None else got[tokens]
     return oracle.rel_frobenius(sel, ref), layer, w
 
@@ -121,7 +123,12 @@ def test_nvfp4_weight_codes_match_oracle():
 
 
 # ------------------------------------------------------- full-size workloads
-FULL = [("qwen3-235b", 256, 24), ("qwen3-235b", 8192, 12), ("qwen35-397b", 64, 8), ("qwen35-397b", 512, 6),
+# Real weights on every expert, compared on a seeded token sample.  The
+# bf16 workload decodes its weights cheaply, so it compares 512 tokens (all
+# of them at T = 256); the NVFP4 workloads re-encode every expert they touch
+# with the oracle's own quantiser (seconds per expert), so they compare a
+# few tokens here and every row of chosen experts in the tests below.
+FULL = [("qwen3-235b", 256, 256), ("qwen3-235b", 8192, 512), ("qwen35-397b", 64, 8), ("qwen35-397b", 512, 6),
         ("qwen35-397b", 4096, 6), ("deepseek-v3", 256, 3), ("deepseek-v3", 16384, 3)]
 
 
@@ -129,17 +136,88 @@ FULL = [("qwen3-235b", 256, 24), ("qwen3-235b", 8192, 12), ("qwen35-397b", 64, 8
 def test_full_size_sampled_tokens(name, T, n):
     cfg = synth.CONFIGS[name]
     toks = synth.sample_tokens(T, n, seed=T)
-    err, *_ = _run(cfg, T, seed=0, tokens=toks)
+    err, *_ = _run(cfg, T, seed=0, tokens=toks, cache=False)
     assert err <= _tol(cfg), err
 
 
+def _chosen_experts(counts, seed, max_rows):
+    """Experts whose every routed row is compared: the hottest (at most
+    max_rows rows: a group split into many token blocks), one whose row count
+    is above 256 and not a multiple of 128 (several blocks and a partial
+    last tile), the one with the fewest rows (fewer than 16 where routing
+    leaves such an expert), and one more drawn at random."""
+    counts = np.asarray(counts)
+    rng = np.random.default_rng(seed)
+    live = np.nonzero(counts)[0]
+    fit = live[counts[live] <= max_rows]
+    chosen = [int(fit[np.argmax(counts[fit])])]
+    ragged = [e for e in fit if counts[e] > 256 and counts[e] % 128 and e not in chosen]
+    if ragged:
+        chosen.append(int(rng.choice(ragged)))
+    small = [e for e in live if e not in chosen]
+    chosen.append(int(min(small, key=lambda e: (counts[e], e))))
+    rest = [e for e in fit if e not in chosen]
+    if rest:
+        chosen.append(int(rng.choice(rest)))
+    return chosen
+
+
+def _run_chosen_experts(cfg, T, seed=0, max_rows=8192, extra_tokens=512):
+    """The whole layer at full size through moe_forward, with the master
+    weights of every expert outside a chosen few set to zero.  Routing,
+    permutation, every tile of the grouped GEMMs (zero experts included) and
+    the combine run as usual; a zero expert contributes exactly zero (in the
+    oracle it is skipped), so each token's output holds its chosen experts'
+    rows and the shared expert.  Compared: every token routed to a chosen
+    expert, plus a seeded sample of others."""
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
+    acts = synth.make_activations(cfg, T, seed=seed)
+    idx, _ = oracle.route(acts.logits.numpy(), cfg.k)
+    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
+    chosen = _chosen_experts(counts, seed + T, max_rows)
+    zero = np.setdiff1d(np.arange(cfg.E), chosen)
+    w = synth.make_weights(cfg, seed=seed, device=DEV)
+    zi = torch.from_numpy(zero).to(DEV)
+    w.w13[zi] = 0
+    w.w2[zi] = 0
+    layer = MoELayer.from_config(cfg, w)
+    out = layer(acts.x.to(DEV), acts.logits.to(DEV))
+    assert moe_sync_status() == 0
+    got = to_np_f32(out)
+    assert np.isfinite(got).all()
+    mine = np.nonzero(np.isin(idx, chosen).any(axis=1))[0]
+    toks = np.union1d(mine, synth.sample_tokens(T, extra_tokens, seed=T + 1))
+    ref, *_ = oracle_layer(cfg, acts, OracleWeights(cfg, w, cache=False, zero_experts=zero), tokens=toks)
+    return oracle.rel_frobenius(got[toks], ref), counts[chosen], len(toks)
+
+
+CHOSEN = [("qwen35-397b", 64), ("qwen35-397b", 512), ("qwen35-397b", 4096), ("deepseek-v3", 256),
+          ("deepseek-v3", 16384), ("qwen3-235b", 8192)]
+
+
+@pytest.mark.parametrize("name,T", CHOSEN)
+def test_full_size_every_row_of_chosen_experts(name, T):
+    cfg = synth.CONFIGS[name]
+    err, rows, ntok = _run_chosen_experts(cfg, T)
+    assert ntok >= min(T, 512)
+    assert err <= _tol(cfg), (err, rows)
+
+
 @pytest.mark.parametrize("w_fmt,zipf,T", [("bf16", 2.0, 1), ("bf16", 0.0, 4096), ("nvfp4", 2.0, 65536),
-                                          ("nvfp4", 0.0, 2)])
+                                          ("nvfp4", 0.0, 2), ("nvfp4", 1.1, 64), ("bf16", 1.1, 16384),
+                                          ("nvfp4", 0.0, 8192)])
 def test_sweep_points(w_fmt, zipf, T):
-    """Size / imbalance sweep on the DeepSeek-V3 shapes (sampled tokens)."""
+    """Size / imbalance sweep on the DeepSeek-V3 shapes.  Few tokens (up to
+    64 with bf16 weights, 2 with NVFP4 weights, whose oracle re-encodes every
+    expert it touches): real weights on every expert, every token compared.
+    Otherwise every row of chosen experts plus a sample of 64 other tokens
+    (all tokens at T = 64), as above."""
     cfg = synth.sweep_config(w_fmt, zipf)
-    toks = synth.sample_tokens(T, 2, seed=T)
-    err, *_ = _run(cfg, T, seed=0, tokens=toks)
+    if T <= (64 if w_fmt == "bf16" else 2):
+        err, *_ = _run(cfg, T, seed=0, cache=False)
+    else:
+        err, rows, ntok = _run_chosen_experts(cfg, T, max_rows=4096, extra_tokens=64)
+        assert ntok >= 64
     assert err <= _tol(cfg), err
 
 
