@@ -115,9 +115,15 @@ def fake_quant(v: np.ndarray, fmt: str) -> np.ndarray:
     return dequantize(q, s, fmt).reshape(v.shape)
 
 
+def round_f32(v: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 (round to nearest even) -> fp64."""
+    return np.asarray(v, dtype=np.float64).astype(F32).astype(np.float64)
+
+
 def h_quant(fmt: str):
     """The MX layers' step between the SwiGLU and the down projection.  The
-    pages leave it open; reading taken: the gate/up GEMM stores h in bf16
-    (round to nearest even) and h is quantised from there, in blocks of 32
-    along I, like the activations."""
-    return lambda h: fake_quant(round_bf16(h), fmt)
+    pages leave it open; reading taken (the same as for the NVFP4
+    activations): h is the SwiGLU output in fp32, the precision of the
+    gate/up GEMM's accumulators, quantised from there in blocks of 32 along I
+    like the activations along H."""
+    return lambda h: fake_quant(round_f32(h), fmt)

@@ -141,8 +141,9 @@ def _h_probe(h_values):
 
 
 def test_mxfp4_h_step_hand_worked():
-    """Block amax 6 -> scale 2^0: h is rounded to the E2M1 grid itself after
-    its bf16 rounding (1.6 -> 1.6015625 -> 1.5, -5.1 -> -5.09375 -> -6)."""
+    """Block amax 6 -> scale 2^0: h (in fp32) is rounded to the E2M1 grid
+    itself, ties to the even code (1.25 -> 1, 2.5 -> 2, 3.5 -> 4, 5 -> 4;
+    1.6 -> 1.5, -5.1 -> -6)."""
     from oracle.moe import expert_mlp
     h = [6.0, 1.25, 3.5, 5.0, 0.25, 2.5, -0.8, 1.6, -4.4, 0.3, 0.0, 2.9, -5.1, 0.7, 1.9, 3.2] + [0.0] * 16
     want = [6.0, 1.0, 4.0, 4.0, 0.0, 2.0, -1.0, 1.5, -4.0, 0.5, 0.0, 3.0, -6.0, 0.5, 2.0, 3.0] + [0.0] * 16
@@ -162,15 +163,18 @@ def test_mxfp8_h_step_hand_worked():
     np.testing.assert_allclose(y, want, rtol=0, atol=1e-12)
 
 
-def test_h_step_rounds_to_bf16_first():
-    """1.2500001 is 1.25 in bf16, a tie between E2M1's 1 and 1.5 that goes to
-    the even code 1; quantising the fp32 value directly would give 1.5."""
+def test_h_step_quantises_the_fp32_value():
+    """h enters the codec as fp32: 1.2500001 (fp32 1.25000012) lies above
+    the E2M1 tie 1.25 and goes to 1.5, where a bf16 rounding first (to 1.25
+    exactly, a tie that goes to the even code 1) would give 1.  And a value
+    that fp32 rounds onto the tie, 1.25 + 2^-30, goes to the even code 1."""
     from oracle.moe import expert_mlp
-    h = [6.0, 1.2500001] + [0.0] * 30
+    h = [6.0, 1.2500001, 1.25 + 2.0**-30] + [0.0] * 29
     a, w13, w2 = _h_probe(h)
     y = expert_mlp(a, w13, w2, h_quant=mx.h_quant("mxfp4"))[0]
-    assert y[1] == 1.0
-    assert mx.fake_quant(np.array([h]), "mxfp4")[0, 1] == 1.5
+    assert y[1] == 1.5
+    assert y[2] == 1.0
+    assert mx.fake_quant(mx.round_bf16(np.array([h])), "mxfp4")[0, 1] == 1.0
 
 
 def test_forward_applies_the_h_step_to_routed_and_shared_experts():
