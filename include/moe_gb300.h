@@ -90,6 +90,9 @@ extern "C" {
                                   C = silu(A W_gate^T) * (A W_up^T), rounded to bf16   */
 #define MOE_EPI_SWIGLU_NVFP4 2 /* as SWIGLU_BF16, but the fp32 result is quantised to
                                   NVFP4 with a caller-given global scale              */
+#define MOE_EPI_SWIGLU_MX 3    /* as SWIGLU_BF16, but the fp32 result is quantised to
+                                  the operands' MX format (moe_quant_mx's recipe,
+                                  blocks of 32 along N)                               */
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int moe_version(void);
@@ -258,7 +261,9 @@ int moe_quant_mx(const uint16_t* x, int rows, int cols, int fmt, uint8_t* codes,
  * SWIGLU_NVFP4 writes C = codes [M_total, N/2] and C_sf [M_total, N/16].
  * MX formats (a_fmt = w_fmt), scales E8M0
  * [.., K/32] (moe_quant_mx), no global scales (A_g, W_g, c_g ignored),
- * STORE_BF16 and SWIGLU_BF16 only:
+ * STORE_BF16, SWIGLU_BF16 and SWIGLU_MX (the MX-only epilogue: C = codes
+ * [M_total, N] (MXFP8) or [M_total, N/2] (MXFP4), C_sf = E8M0 [M_total,
+ * N/32]):
  *   MOE_FMT_MXFP4: codes as NVFP4; K % 512 == 0, 16-byte aligned scales
  *   MOE_FMT_MXFP8: E4M3 bytes [.., K]; K % 256 == 0, 8-byte aligned scales
  * The kernel is persistent (one CTA per SM), reads offsets on the device,
@@ -336,7 +341,7 @@ int moe_shared_gate(const uint16_t* x, const uint16_t* g, int T, int H,
  *                  (w13 [E, 2I, H or H/2], w2 [E, H, I or I/2]), scales E8M0
  *                  [.., K/32], no global scales (*_g, g_h, g_hs ignored); x
  *                  and h are quantised the same way inside the layer, h from
- *                  its bf16 value.  H, I, I_s multiples of 512 (MXFP4) or 256
+ *                  its fp32 value in the gate/up GEMM's epilogue.  H, I, I_s multiples of 512 (MXFP4) or 256
  *                  (MXFP8).
  * I_s = 0 means no shared expert.
  * Variants (zero-initialised fields keep the default layer):

@@ -29,6 +29,7 @@ MOE_FMT_MXFP4 = 3
 MOE_EPI_STORE_BF16 = 0
 MOE_EPI_SWIGLU_BF16 = 1
 MOE_EPI_SWIGLU_NVFP4 = 2
+MOE_EPI_SWIGLU_MX = 3
 
 
 class MoeLayerC(ctypes.Structure):

@@ -11,7 +11,7 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import (MOE_EPI_STORE_BF16, MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_NVFP4, MOE_FMT_BF16, MOE_FMT_MXFP4,
+from ._lib import (MOE_EPI_STORE_BF16, MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_MX, MOE_EPI_SWIGLU_NVFP4, MOE_FMT_BF16, MOE_FMT_MXFP4,
                    MOE_FMT_MXFP8, MOE_FMT_NVFP4, check, load)
 
 
@@ -237,7 +237,8 @@ def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tenso
     _dev(offsets, "offsets", dtype=torch.int32, device=dev)
     G = offsets.numel() - 1
     M = A.shape[0]
-    wn = 2 * N if epilogue in (MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_NVFP4) else N
+    wn = 2 * N if epilogue in (MOE_EPI_SWIGLU_BF16, MOE_EPI_SWIGLU_NVFP4, MOE_EPI_SWIGLU_MX) else N
+    mx_c = N // 2 if a_fmt == MOE_FMT_MXFP4 else N  # bytes per row of MX-coded C
     _dev(W, "W", device=dev)
     if a_fmt == MOE_FMT_NVFP4:
         _at_least(A, "A", M * K // 2)
@@ -267,6 +268,9 @@ def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tenso
         if epilogue == MOE_EPI_SWIGLU_NVFP4:
             C = torch.empty(M, N // 2, dtype=torch.uint8, device=dev)
             C_sf = torch.empty(M, N // 16, dtype=torch.uint8, device=dev)
+        elif epilogue == MOE_EPI_SWIGLU_MX:
+            C = torch.empty(M, mx_c, dtype=torch.uint8, device=dev)
+            C_sf = torch.empty(M, N // 32, dtype=torch.uint8, device=dev)
         else:
             C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     _dev(C, "C", device=dev)
@@ -276,12 +280,16 @@ def moe_grouped_gemm(a_fmt: int, w_fmt: int, epilogue: int, offsets: torch.Tenso
         _at_least(C_sf, "C_sf", M * N // 16)
         _dev(c_g, "c_g", dtype=torch.float32, device=dev)
         _at_least(c_g, "c_g", 4)
+    elif epilogue == MOE_EPI_SWIGLU_MX:
+        _at_least(C, "C", M * mx_c)
+        _dev(C_sf, "C_sf", device=dev)
+        _at_least(C_sf, "C_sf", M * N // 32)
     else:
         _at_least(C, "C", M * N * 2)
     check(load().moe_grouped_gemm(a_fmt, w_fmt, epilogue, G, _ptr(offsets), M, N, K, _ptr(A), _ptr(A_sf),
                                   _ptr(A_g), _ptr(W), _ptr(W_sf), _ptr(W_g), _ptr(C), _ptr(C_sf), _ptr(c_g),
                                   _stream(stream)), "moe_grouped_gemm")
-    return (C, C_sf) if epilogue == MOE_EPI_SWIGLU_NVFP4 else C
+    return (C, C_sf) if epilogue in (MOE_EPI_SWIGLU_NVFP4, MOE_EPI_SWIGLU_MX) else C
 
 
 def moe_combine(Y: torch.Tensor, row_of: torch.Tensor, w: torch.Tensor, Ys: Optional[torch.Tensor],

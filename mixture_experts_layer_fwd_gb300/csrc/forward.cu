@@ -36,11 +36,6 @@ struct FwdBufs {
   uint16_t* Y;
   uint16_t* Ys;
   float* gate;  // shared-expert gate per token (gated layers)
-  // MX layers: h (bf16, in `h` / `hs`) quantised for the down projection
-  uint8_t* hq;
-  uint8_t* hq_sf;
-  uint8_t* hsq;
-  uint8_t* hsq_sf;
 };
 
 inline bool is_mx(int fmt) { return fmt == MOE_FMT_MXFP4 || fmt == MOE_FMT_MXFP8; }
@@ -100,20 +95,17 @@ size_t carve(const moe_layer* L, int T, void* ws, size_t cap, FwdBufs* b) {
   b->xp_sf = b->h_sf = b->hs_sf = nullptr;
   b->hs = nullptr;
   b->Ys = nullptr;
-  b->hq = b->hq_sf = b->hsq = b->hsq_sf = nullptr;
   if (is_mx(L->w_fmt)) {
     const int f = L->w_fmt;
     b->xq = c.take<uint8_t>(mx_code_bytes(f, static_cast<size_t>(T) * L->H));
     b->xsf = c.take<uint8_t>(static_cast<size_t>(T) * L->H / 32);
     b->xp = c.take<uint8_t>(mx_code_bytes(f, Tk * L->H));
     b->xp_sf = c.take<uint8_t>(Tk * L->H / 32);
-    b->h = c.take<uint16_t>(Tk * L->I);
-    b->hq = c.take<uint8_t>(mx_code_bytes(f, Tk * L->I));
-    b->hq_sf = c.take<uint8_t>(Tk * L->I / 32);
+    b->h = c.take<uint8_t>(mx_code_bytes(f, Tk * L->I));
+    b->h_sf = c.take<uint8_t>(Tk * L->I / 32);
     if (L->I_s) {
-      b->hs = c.take<uint16_t>(static_cast<size_t>(T) * L->I_s);
-      b->hsq = c.take<uint8_t>(mx_code_bytes(f, static_cast<size_t>(T) * L->I_s));
-      b->hsq_sf = c.take<uint8_t>(static_cast<size_t>(T) * L->I_s / 32);
+      b->hs = c.take<uint8_t>(mx_code_bytes(f, static_cast<size_t>(T) * L->I_s));
+      b->hs_sf = c.take<uint8_t>(static_cast<size_t>(T) * L->I_s / 32);
     }
   } else if (a4) {
     b->xq = c.take<uint8_t>(static_cast<size_t>(T) * L->H / 2);
@@ -197,9 +189,8 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
   if (b.gate) MOE_TRY(shared_gate_launch(x, L->ws_gate, T, H, b.gate, s));
   MOE_TRY(mark(events, 1, s));
   if (is_mx(L->w_fmt)) {
-    // MX layers: x quantised in blocks of 32 along H; the GEMMs keep h in
-    // bf16, which is quantised the same way along I before the down
-    // projection (inside the gate/up window of the stage events)
+    // MX layers: x quantised in blocks of 32 along H; the gate/up GEMM's
+    // epilogue quantises h the same way along I from its fp32 value
     const int f = L->w_fmt;
     const int I = L->I, I_s = L->I_s;
     MOE_TRY(moe_quant_mx(x, T, H, f, b.xq, b.xsf, stream));
@@ -207,14 +198,12 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const
     MOE_TRY(permute_launch(b.idx, T, k, E, b.xq, static_cast<int>(mx_code_bytes(f, H)), b.xsf, H / 32, b.counts,
                            b.offsets, b.row_of, b.src_tok, b.xp, b.xp_sf, b.perm_ws, b.perm_ws_bytes, s));
     MOE_TRY(mark(events, 3, s));
-    GemmProblem r1{b.xp, b.xp_sf, nullptr, Tk, L->w13, L->w13_sf, nullptr, E, b.h, nullptr, nullptr, I, H};
-    GemmProblem s1{b.xq, b.xsf, nullptr, T, L->ws13, L->ws13_sf, nullptr, 1, b.hs, nullptr, nullptr, I_s, H};
-    MOE_TRY(grouped_gemm_launch(MOE_EPI_SWIGLU_BF16, f, f, r1, b.offsets, E, I_s ? &s1 : nullptr, T, s));
-    MOE_TRY(moe_quant_mx(static_cast<const uint16_t*>(b.h), Tk, I, f, b.hq, b.hq_sf, stream));
-    if (I_s) MOE_TRY(moe_quant_mx(static_cast<const uint16_t*>(b.hs), T, I_s, f, b.hsq, b.hsq_sf, stream));
+    GemmProblem r1{b.xp, b.xp_sf, nullptr, Tk, L->w13, L->w13_sf, nullptr, E, b.h, b.h_sf, nullptr, I, H};
+    GemmProblem s1{b.xq, b.xsf, nullptr, T, L->ws13, L->ws13_sf, nullptr, 1, b.hs, b.hs_sf, nullptr, I_s, H};
+    MOE_TRY(grouped_gemm_launch(MOE_EPI_SWIGLU_MX, f, f, r1, b.offsets, E, I_s ? &s1 : nullptr, T, s));
     MOE_TRY(mark(events, 4, s));
-    GemmProblem r2{b.hq, b.hq_sf, nullptr, Tk, L->w2, L->w2_sf, nullptr, E, b.Y, nullptr, nullptr, H, I};
-    GemmProblem s2{b.hsq, b.hsq_sf, nullptr, T, L->ws2, L->ws2_sf, nullptr, 1, b.Ys, nullptr, nullptr, H, I_s};
+    GemmProblem r2{b.h, b.h_sf, nullptr, Tk, L->w2, L->w2_sf, nullptr, E, b.Y, nullptr, nullptr, H, I};
+    GemmProblem s2{b.hs, b.hs_sf, nullptr, T, L->ws2, L->ws2_sf, nullptr, 1, b.Ys, nullptr, nullptr, H, I_s};
     MOE_TRY(grouped_gemm_launch(MOE_EPI_STORE_BF16, f, f, r2, b.offsets, E, I_s ? &s2 : nullptr, T, s));
     MOE_TRY(mark(events, 5, s));
     MOE_TRY(combine_launch(b.Y, b.row_of, b.w, b.Ys, b.gate, T, k, H, out, s));

@@ -437,10 +437,11 @@ static int check_problem(int epi, bool a4, bool w4, const GemmProblem& P) {
 // per 32 elements, no global scales.  The MXFP4 kernel stages 16 scale bytes
 // per row by TMA (K % 512, 16-byte aligned scales); the MXFP8 kernel loads 8
 // per row directly (K % 256, 8-byte aligned scales).
-static int check_problem_mx(const GemmProblem& P, bool fp8) {
+static int check_problem_mx(const GemmProblem& P, bool fp8, bool mx_out) {
   if (P.N <= 0 || P.K <= 0 || P.a_rows < 0 || P.groups < 1) return MOE_ERR_INVALID_ARG;
   if (P.K % (fp8 ? 256 : 512) != 0 || P.N % 32 != 0) return MOE_ERR_UNSUPPORTED;
   if (!P.A || !P.W || !P.C || !P.A_sf || !P.W_sf) return MOE_ERR_INVALID_ARG;
+  if (mx_out && !P.C_sf) return MOE_ERR_INVALID_ARG;
   const int sfa = fp8 ? 8 : 16;
   if (!aligned(P.A, 16) || !aligned(P.W, 16) || !aligned(P.C, 16) || !aligned(P.A_sf, sfa) || !aligned(P.W_sf, sfa))
     return MOE_ERR_INVALID_ARG;
@@ -455,13 +456,15 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
   const bool mx8 = a_fmt == MOE_FMT_MXFP8 || w_fmt == MOE_FMT_MXFP8;
   if (mx8 || a_fmt == MOE_FMT_MXFP4 || w_fmt == MOE_FMT_MXFP4) {
     if (a_fmt != w_fmt) return MOE_ERR_UNSUPPORTED;
-    if (epi != MOE_EPI_STORE_BF16 && epi != MOE_EPI_SWIGLU_BF16) return MOE_ERR_UNSUPPORTED;
-    MOE_TRY(check_problem_mx(routed, mx8));
-    if (sh) MOE_TRY(check_problem_mx(*sh, mx8));
+    if (epi != MOE_EPI_STORE_BF16 && epi != MOE_EPI_SWIGLU_BF16 && epi != MOE_EPI_SWIGLU_MX)
+      return MOE_ERR_UNSUPPORTED;
+    MOE_TRY(check_problem_mx(routed, mx8, epi == MOE_EPI_SWIGLU_MX));
+    if (sh) MOE_TRY(check_problem_mx(*sh, mx8, epi == MOE_EPI_SWIGLU_MX));
     if (routed.a_rows == 0) return MOE_OK;
     if (mx8) return grouped_gemm_launch_mxf8(epi, routed, offsets, G, sh, shared_rows, s);
     return grouped_gemm_launch_mxf4(epi, routed, offsets, G, sh, shared_rows, s);
   }
+  if (epi == MOE_EPI_SWIGLU_MX) return MOE_ERR_UNSUPPORTED;  // MX operands only
   if ((epi < MOE_EPI_STORE_BF16 || epi > MOE_EPI_SWIGLU_NVFP4) && epi != kEpiSwigluF16) return MOE_ERR_INVALID_ARG;
   if (a4 && !w4) return MOE_ERR_UNSUPPORTED;
   if (epi == kEpiSwigluF16 && (a4 || !w4)) return MOE_ERR_UNSUPPORTED;
@@ -513,7 +516,7 @@ extern "C" int moe_grouped_gemm(int a_fmt, int w_fmt, int epilogue, int G, const
                                 const uint8_t* W_sf, const float* W_g, void* C, uint8_t* C_sf, const float* c_g,
                                 void* stream) {
   if (M_total < 0) return MOE_ERR_INVALID_ARG;
-  if (epilogue < MOE_EPI_STORE_BF16 || epilogue > MOE_EPI_SWIGLU_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (epilogue < MOE_EPI_STORE_BF16 || epilogue > MOE_EPI_SWIGLU_MX) return MOE_ERR_INVALID_ARG;
   if (M_total == 0) return MOE_OK;
   GemmProblem P{A, A_sf, A_g, M_total, W, W_sf, W_g, G, C, C_sf, c_g, N, K};
   return grouped_gemm_launch(epilogue, a_fmt, w_fmt, P, offsets, G, nullptr, 0, static_cast<cudaStream_t>(stream));

@@ -129,7 +129,9 @@ DEVINL float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 // bf16 or quantised to NVFP4 with global scale *P.c_g.
 // Every lane of the warp must call it (tcgen05.ld is warp-collective); only
 // rows inside the tile's group are stored.
-template <int EPI, int ACC_N>
+// SWIGLU_MX: the result is quantised to MXFP4 (MX_FP4) or MXFP8, one E8M0
+// scale per 32 columns (one tensor-memory chunk of a row).
+template <int EPI, int ACC_N, bool MX_FP4 = false>
 DEVINL void epilogue_tile(const Prob& P, const TileInfo& ti, uint32_t taddr, int r_in_tile, float scale) {
   const int m_local = ti.m_blk * BM + r_in_tile;
   const bool valid = m_local < ti.rows;
@@ -175,6 +177,18 @@ DEVINL void epilogue_tile(const Prob& P, const TileInfo& ti, uint32_t taddr, int
           for (int v = 0; v < 4; ++v)
             dst[v] = make_uint4(pack_bf16x2(h[8 * v], h[8 * v + 1]), pack_bf16x2(h[8 * v + 2], h[8 * v + 3]),
                                 pack_bf16x2(h[8 * v + 4], h[8 * v + 5]), pack_bf16x2(h[8 * v + 6], h[8 * v + 7]));
+        } else if (EPI == MOE_EPI_SWIGLU_MX) {
+          uint32_t q[MX_FP4 ? 4 : 8];
+          const uint32_t sc = mx_quantize32<MX_FP4>(h, q);
+          if constexpr (MX_FP4) {
+            *reinterpret_cast<uint4*>(static_cast<uint8_t*>(P.c) + row * (P.n_out / 2) + col / 2) =
+                make_uint4(q[0], q[1], q[2], q[3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(P.c) + row * P.n_out + col);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+          }
+          P.c_sf[row * (P.n_out / 32) + col / 32] = static_cast<uint8_t>(sc);
         } else {
           float b0[16], b1[16];
 #pragma unroll

@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8_kernel(const __g
       if (!mbar_wait_warp(&tfull[buf], use & 1u, tmo, p.err, abort_flag)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      gg::epilogue_tile<EPI, BN>(P, ti, taddr, r_in_tile, 1.0f);
+      gg::epilogue_tile<EPI, BN, false>(P, ti, taddr, r_in_tile, 1.0f);
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }
@@ -373,7 +373,7 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
   q.a_rows = P.a_rows;
   q.w_rows_total = P.groups * q.w_rows;
   q.c = P.C;
-  q.c_sf = nullptr;
+  q.c_sf = P.C_sf;  // MX codes of h (SWIGLU_MX)
   q.a_g = q.w_g = q.c_g = nullptr;
   q.a_sf = P.A_sf;
   q.w_sf = P.W_sf;
@@ -404,7 +404,7 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
 
 }  // namespace gmx8
 
-// MXFP8 x MXFP8, K % 256 == 0, 8-byte aligned scale arrays, bf16 epilogues
+// MXFP8 x MXFP8, K % 256 == 0, 8-byte aligned scale arrays, bf16 and MX SwiGLU epilogues
 // (checked by the caller, grouped_gemm_launch).
 int grouped_gemm_launch_mxf8(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                              const GemmProblem* sh, int shared_rows, cudaStream_t s) {
@@ -422,6 +422,7 @@ int grouped_gemm_launch_mxf8(int epi, const GemmProblem& routed, const int32_t* 
   if (!prm.err) return MOE_ERR_CUDA;
   prm.timeout_ns = wait_timeout_ns();
   if (epi == MOE_EPI_STORE_BF16) return gmx8::launch<MOE_EPI_STORE_BF16>(prm, s);
+  if (epi == MOE_EPI_SWIGLU_MX) return gmx8::launch<MOE_EPI_SWIGLU_MX>(prm, s);
   return gmx8::launch<MOE_EPI_SWIGLU_BF16>(prm, s);
 }
 

@@ -1,6 +1,7 @@
 // NVFP4 helpers of the CUDA path: E4M3 scale encode/decode, E2M1 code
 // selection, and the 16-element block quantiser shared by the activation
-// quantiser and the NVFP4 SwiGLU epilogue of the grouped GEMM.
+// quantiser and the NVFP4 SwiGLU epilogue of the grouped GEMM; the
+// 32-element MX block quantiser of the MX SwiGLU epilogue.
 //
 // Format ("Driving vLLM WideEP and Large-Scale Serving Toward Maturity on
 // Blackwell (Part I)", sections "NVFP4 GEMM for MoE and O-proj" and "NVFP4
@@ -59,6 +60,37 @@ DEVINL uint32_t nvfp4_quantize16(const float (&v)[16], float g, uint32_t (&codes
     codes[i >> 3] |= code << (4 * (i & 7));
   }
   return s;
+}
+
+// One MX block of 32 fp32 values (moe_quant_mx's recipe): E8M0 scale
+// exponent e = floor(log2 amax) - emax (emax 2 for E2M1, 8 for E4M3),
+// clamped to [-127, 127], read from the abs-max's exponent field (a zero or
+// subnormal abs-max gives -127); elements RNE_satfinite(v * 2^-e) with the
+// sign kept.  2^-e is a normal fp32 because a finite amax has exponent
+// field <= 254, so the scaling is exact unless the product underflows.
+// Returns the E8M0 byte; codes: FP4 -> 4 words of packed E2M1 (element 2j
+// in the low nibble of byte j), FP8 -> 8 words of E4M3 bytes.
+template <bool FP4>
+DEVINL uint32_t mx_quantize32(const float (&v)[32], uint32_t (&codes)[FP4 ? 4 : 8]) {
+  constexpr int EMAX = FP4 ? 2 : 8;
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = max(-127, min(127, static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - EMAX));
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+  for (int w = 0; w < (FP4 ? 4 : 8); ++w) codes[w] = 0u;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float x = v[i] * inv;
+    if (FP4) {
+      const uint32_t code = e2m1_magnitude(fabsf(x)) | ((__float_as_uint(v[i]) >> 31) << 3);
+      codes[i >> 3] |= code << (4 * (i & 7));
+    } else {
+      codes[i >> 2] |= e4m3_encode_satfinite(x) << (8 * (i & 3));
+    }
+  }
+  return static_cast<uint32_t>(e + 127);
 }
 
 // bf16 bit pattern of each E2M1 code (sign in bit 3).

@@ -64,3 +64,34 @@ def test_grouped_gemm_mx(fmt, epi, N, K, counts):
     got = C.float().cpu().numpy()
     err = oracle.rel_frobenius(got, ref)
     assert err < 5e-3, err
+
+
+@pytest.mark.parametrize("fmt,N,K,counts", [
+    ("mxfp4", 128, 512, [128]),
+    ("mxfp4", 256, 1536, [300, 0, 513, 257, 64, 130]),
+    ("mxfp8", 128, 256, [128]),
+    ("mxfp8", 192, 1280, [7, 0, 260, 129]),
+])
+def test_grouped_gemm_mx_swiglu_mx_epilogue(fmt, N, K, counts):
+    """SWIGLU_MX: the epilogue quantises the fp32 SwiGLU output to the MX
+    format (blocks of 32 along N).  Compared with the oracle's h step on the
+    exact product (oracle.mx.h_quant): codes that sit on a rounding boundary
+    may flip between the fp32 and fp64 values, so the decoded values are
+    compared by relative Frobenius error."""
+    import mixture_experts_layer_fwd_gb300 as m
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M, G = int(offs[-1]), len(counts)
+    g = torch.Generator().manual_seed(N + K + 7)
+    x = (torch.randn(M, K, generator=g) * torch.exp(torch.randn(M, 1, generator=g))).numpy()
+    Aq, As = mx.quantize(x, fmt)
+    Wq, Ws = zip(*[mx.quantize((torch.randn(2 * N, K, generator=g) * 0.05).numpy(), fmt) for _ in range(G)])
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    Cq, Cs = m.moe_grouped_gemm(FMT[fmt], FMT[fmt], m.MOE_EPI_SWIGLU_MX, t(offs), N, K, t(Aq), t(np.stack(Wq)),
+                                A_sf=t(As), W_sf=t(np.stack(Ws)))
+    assert m.moe_sync_status() == 0
+    Ad = mx.dequantize(Aq, As, fmt)
+    Wd = np.stack([mx.dequantize(q, s, fmt) for q, s in zip(Wq, Ws)])
+    ref = mx.h_quant(fmt)(_ref(Ad, Wd, offs, True, N))
+    got = mx.dequantize(Cq.cpu().numpy(), Cs.cpu().numpy(), fmt)
+    err = oracle.rel_frobenius(got, ref)
+    assert err < 2e-2 if fmt == "mxfp4" else err < 5e-3, err

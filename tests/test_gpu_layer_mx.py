@@ -1,6 +1,6 @@
 """MX layers (MXFP8 and MXFP4 weights and activations) through moe_forward
 against the fp64 oracle on every token: x quantised in blocks of 32 along
-H, h rounded to bf16 and quantised the same way along I, weights encoded by
+H, h quantised the same way along I from its fp32 value, weights encoded by
 the oracle's own MX codec from the bf16 masters.  Tolerance 1e-2 relative
 Frobenius (as for the NVFP4 layers)."""
 import dataclasses
