@@ -294,19 +294,37 @@ def roofline(cfg, T, gemm_ms, active, traffic, src):
 
 
 # ------------------------------------------------------------------ oracle
-def oracle_tokens_per_s(cfg, acts, w_host, tokens):
-    """Time the fp64 oracle (as it stands) on `tokens` of the workload."""
+# One method for both CPU legs (the GPU arm's cpu_baseline and --impl
+# reference): the oracle's expert weights are widened to fp64 once, before
+# any timing (as the GPU path's weights are prepared once), and each timed
+# step runs oracle.forward on a fresh seeded sample of ORACLE_SAMPLE tokens
+# of the T = 8192 batch.  Every output row depends only on its own token, so
+# a sample is exact work of the workload; tokens/s = sampled tokens / time.
+ORACLE_SAMPLE = 512
+
+
+def oracle_experts(w_host):
+    """fp64 ExpertWeights of every expert, from the bf16 masters on the host."""
     import oracle
     w13, w2 = w_host
+    return [oracle.ExpertWeights(w13[e].double().numpy(), w2[e].double().numpy()) for e in range(w13.shape[0])]
 
-    def get_expert(e):
-        return oracle.ExpertWeights(w13[e].double().numpy(), w2[e].double().numpy())
 
+def oracle_step_s(cfg, acts, experts, tokens):
+    """Seconds of one oracle.forward (as it stands) over `tokens`."""
+    import oracle
     x = acts.x.double().numpy()
+    logits = acts.logits.numpy()
     t0 = time.perf_counter()
-    oracle.forward(x, acts.logits.numpy(), cfg.k, cfg.E, get_expert, None, tokens=tokens)
-    dt = time.perf_counter() - t0
-    return len(tokens) / dt, dt
+    oracle.forward(x, logits, cfg.k, cfg.E, lambda e: experts[e], None, tokens=tokens)
+    return time.perf_counter() - t0
+
+
+def oracle_run(cfg, T, acts, experts, steps, seed0):
+    """`steps` oracle steps on fresh samples; returns (tokens/s, seconds per step)."""
+    times = [oracle_step_s(cfg, acts, experts, synth.sample_tokens(T, ORACLE_SAMPLE, seed=seed0 + i))
+             for i in range(steps)]
+    return ORACLE_SAMPLE * steps / sum(times), times
 
 
 def cpu_threads() -> int:
@@ -320,9 +338,14 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
+def oracle_sample_note(T, steps):
+    return (f"{steps} steps of {ORACLE_SAMPLE} seeded tokens of the T={T} batch (fresh sample per step; "
+            f"rows are token-independent), expert weights widened to fp64 once before timing")
+
+
 def run_reference(args):
-    """--impl reference: the CPU oracle on the bench workload, K timed steps
-    of bounded token samples."""
+    """--impl reference: the CPU oracle on the bench workload, W + K steps
+    of the oracle method above."""
     # rank 0 alone runs the oracle; the other ranks exit without work and
     # without joining a process group
     if int(os.environ.get("RANK", "0")) != 0:
@@ -330,39 +353,86 @@ def run_reference(args):
     cfg, T = CFG, T_MAIN
     acts = synth.make_activations(cfg, T, seed=0)
     w = synth.make_weights(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
-    w_host = (w.w13.cpu(), w.w2.cpu())
+    experts = oracle_experts((w.w13.cpu(), w.w2.cpu()))
     del w
-    # size the per-step sample so that warmup + steps take about 3 minutes:
-    # a step costs a fixed part (the routed experts' weights widened to fp64)
-    # plus a part per token, so probe two sample sizes and solve for n
-    _, t8 = oracle_tokens_per_s(cfg, acts, w_host, synth.sample_tokens(T, 8, seed=1))
-    _, t64 = oracle_tokens_per_s(cfg, acts, w_host, synth.sample_tokens(T, 64, seed=2))
-    per_tok = max((t64 - t8) / 56.0, 1e-6)
-    fixed = max(t64 - 64 * per_tok, 0.0)
-    budget = 180.0 / max(1, args.steps + args.warmup)
-    n = int(max(8, min(T, (budget - fixed) / per_tok)))
-    times = []
-    for i in range(args.warmup + args.steps):
-        toks = synth.sample_tokens(T, n, seed=100 + i)
-        _, dt = oracle_tokens_per_s(cfg, acts, w_host, toks)
-        if i >= args.warmup:
-            times.append(dt)
-    value = n * args.steps / sum(times)
+    oracle_run(cfg, T, acts, experts, args.warmup, seed0=100)
+    value, times = oracle_run(cfg, T, acts, experts, args.steps, seed0=100 + args.warmup)
     line = {
         "impl": "reference", "metric": metric_name(cfg, T), "value": round(value, 3), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * sum(times) / args.steps, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{cfg.name} moe layer bf16 weights, T={T} (oracle on {n}-token samples)",
+        "config": {"workload": f"{cfg.name} moe layer bf16 weights, T={T} (oracle on {ORACLE_SAMPLE}-token "
+                               f"samples)",
                    "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "T": T, "zipf": cfg.zipf},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"{n} seeded tokens of the T={T} batch per step (rows are token-independent)"},
+                         "sample": oracle_sample_note(T, args.steps)},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ GPU arm
+# The NVFP4 workloads measured on the default run besides the benchmark
+# line's own (each carries its own roofline): the Qwen3.5-397B-shaped layer
+# (NVFP4 weights, bf16 activations) at decode and prefill sizes and the
+# DeepSeek-V3-shaped layer (NVFP4 weights and activations).
+EXTRA_POINTS = (("qwen35-397b", (64, 512, 4096)), ("deepseek-v3", (256, 16384)))
+EXTRA_STEPS = 20
+STAGES = ["route", "quant", "permute", "gemm_gate_up", "gemm_down", "combine"]
+
+
+def new_events():
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    for ev in evs:
+        ev.record()  # creates the underlying CUDA events
+    return evs
+
+
+def timed_steps(api, layer, x, logits, out, ws, flush, steps, warmup, evsets=None):
+    """warmup + steps forwards (moe_forward_profiled), L2 flushed before each
+    (outside the events).  Returns the per-step event sets of the timed ones."""
+    warm = new_events()
+    for _ in range(warmup):
+        flush.zero_()
+        api.moe_forward_profiled(layer.c, x, logits, out, ws, warm)
+    evsets = evsets or [new_events() for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        api.moe_forward_profiled(layer.c, x, logits, out, ws, evsets[i])
+    torch.cuda.synchronize()
+    return evsets
+
+
+def stage_table(evsets):
+    return np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(6)] for evs in evsets])
+
+
+def active_experts(api, logits, cfg):
+    idx, _ = api.moe_route(logits, cfg.k)
+    return int((torch.bincount(idx.reshape(-1).long(), minlength=cfg.E) > 0).sum())
+
+
+def measure_point(api, moe_sync_status, layer, cfg, T, dev, flush, steps, warmup, src):
+    """One workload point: mean step time, stage times and the grouped-GEMM
+    roofline over `steps` timed forwards."""
+    acts = synth.make_activations(cfg, T, seed=0)
+    x, logits = acts.x.to(dev), acts.logits.to(dev)
+    out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
+    ws = layer.workspace(T)
+    evsets = timed_steps(api, layer, x, logits, out, ws, flush, steps, warmup)
+    if moe_sync_status() != 0:
+        raise RuntimeError(f"device status not clean at {cfg.name} T={T}")
+    st = stage_table(evsets)
+    ms = float(np.mean([evs[0].elapsed_time(evs[6]) for evs in evsets]))
+    gemm_ms = float(np.mean(st[:, 3] + st[:, 4]))
+    active = active_experts(api, logits, cfg)
+    return {"ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "active_experts": active,
+            "roofline": roofline(cfg, T, gemm_ms, active, None, src),
+            "stage_ms": {n: round(float(np.mean(st[:, i])), 4) for i, n in enumerate(STAGES)}}
+
+
 def run_gpu(args):
     from mixture_experts_layer_fwd_gb300 import MoELayer, api, moe_sync_status
     from mixture_experts_layer_fwd_gb300 import build as _build
@@ -381,24 +451,14 @@ def run_gpu(args):
     w = synth.make_weights(cfg, seed=0, device=str(dev))
     layer = MoELayer.from_config(cfg, w)
     keep_master = rank == 0 and world == 1 and is_main and not args.no_cpu_baseline
-    if cfg.w_fmt == "nvfp4" or not keep_master:
-        w_host = (w.w13.cpu(), w.w2.cpu()) if keep_master else None
-        if cfg.w_fmt == "nvfp4":
-            del w  # the layer holds the NVFP4 weights; free the bf16 master
-            torch.cuda.empty_cache()
-    else:
-        w_host = None
+    w_host = (w.w13.cpu(), w.w2.cpu()) if keep_master else None
+    del w  # the layer holds its own copy or encoding of the weights
+    torch.cuda.empty_cache()
     x = acts.x.to(dev)
     logits = acts.logits.to(dev)
     out = torch.empty(T, cfg.H, dtype=torch.bfloat16, device=dev)
     ws = layer.workspace(T)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-
-    def new_events():
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-        for ev in evs:
-            ev.record()  # creates the underlying CUDA events
-        return evs
 
     evsets = [new_events() for _ in range(args.steps)]
     warm = new_events()
@@ -438,16 +498,12 @@ def run_gpu(args):
     step_ms = [evs[0].elapsed_time(evs[6]) for evs in evsets]
     if graph is not None:
         # per-stage times of the same forward, launched stage by stage
-        for i in range(args.steps):
-            flush.zero_()
-            api.moe_forward_profiled(layer.c, x, logits, out, ws, evsets[i])
-        torch.cuda.synchronize()
-    stage_ms = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(6)] for evs in evsets])
+        timed_steps(api, layer, x, logits, out, ws, flush, args.steps, 0, evsets)
+    stage_ms = stage_table(evsets)
     value, total_s = job_rate(T * args.steps, float(sum(step_ms)) / 1e3, world, dev)
     total_ms = total_s * 1e3
 
-    idx, _ = api.moe_route(logits, cfg.k)
-    active = int((torch.bincount(idx.reshape(-1).long(), minlength=cfg.E) > 0).sum())
+    active = active_experts(api, logits, cfg)
     gemm_ms = float(np.mean(stage_ms[:, 3] + stage_ms[:, 4]))
     _, src = peaks()
     roof = roofline(cfg, T, gemm_ms, active, gemm_traffic_per_launch() if is_main else None, src)
@@ -483,8 +539,7 @@ def run_gpu(args):
                    "l2": "flushed before every step (256 MB write, outside the events)",
                    "parallelism": f"replicas x{world}", "cuda_graph": bool(args.graph)},
         "roofline": roof,
-        "stage_ms": {n: round(float(np.mean(stage_ms[:, i])), 4) for i, n in
-                     enumerate(["route", "quant", "permute", "gemm_gate_up", "gemm_down", "combine"])},
+        "stage_ms": {n: round(float(np.mean(stage_ms[:, i])), 4) for i, n in enumerate(STAGES)},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
                 "h2d_bytes_per_step": T * cfg.H * 2 + T * cfg.E * 4, "d2h_bytes_per_step": T * cfg.H * 2},
         "gpu_launches": launches * args.steps,
@@ -493,30 +548,33 @@ def run_gpu(args):
 
     if is_main:
         # decode-size point on the same weights (weight-streaming bound)
-        Td = T_DECODE
-        xd_, ld_, od_ = x[:Td].contiguous(), logits[:Td].contiguous(), out[:Td]
-        evd = new_events()
-        dec = []
-        for i in range(args.warmup + 10):
-            flush.zero_()
-            api.moe_forward_profiled(layer.c, xd_, ld_, od_, ws, evd)
-            torch.cuda.synchronize()
-            if i >= args.warmup:
-                dec.append((evd[0].elapsed_time(evd[6]), evd[3].elapsed_time(evd[5])))
-        idx_d, _ = api.moe_route(ld_, cfg.k)
-        act_d = int((torch.bincount(idx_d.reshape(-1).long(), minlength=cfg.E) > 0).sum())
-        dec_ms = float(np.median([d[0] for d in dec]))
-        dec_gemm = float(np.median([d[1] for d in dec]))
-        line["decode_T256"] = {"ms": round(dec_ms, 4), "tokens_per_s": round(Td / (dec_ms / 1e3), 1),
-                               "roofline": roofline(cfg, Td, dec_gemm, act_d, None, src)}
+        line["decode_T256"] = measure_point(api, moe_sync_status, layer, cfg, T_DECODE, dev, flush, 10,
+                                            args.warmup, src)
+    del layer, ws, out
+    torch.cuda.empty_cache()
+    if is_main and world == 1 and not args.no_extra:
+        # the NVFP4 workloads, each point with its own roofline
+        for name, Ts in EXTRA_POINTS:
+            c = synth.CONFIGS[name]
+            wc = synth.make_weights(c, seed=0, device=str(dev))
+            lc = MoELayer.from_config(c, wc)
+            del wc
+            torch.cuda.empty_cache()
+            for Tc in Ts:
+                line[f"{name}_T{Tc}"] = measure_point(api, moe_sync_status, lc, c, Tc, dev, flush, EXTRA_STEPS,
+                                                      args.warmup, src)
+            del lc
+            torch.cuda.empty_cache()
     if keep_master:
-        if w_host is None:
-            w_host = (w.w13.cpu(), w.w2.cpu())
-        toks = synth.sample_tokens(T, args.cpu_tokens, seed=1)
-        r, dt = oracle_tokens_per_s(cfg, acts, w_host, toks)
+        experts = oracle_experts(w_host)
+        del w_host
+        steps = 0
+        r, times = oracle_run(cfg, T, acts, experts, 1, seed0=1)
+        # about 10-30 s of CPU work: as many sample steps as fit in ~15 s
+        steps = max(1, min(30, int(15.0 / max(times[0], 1e-3))))
+        r, times = oracle_run(cfg, T, acts, experts, steps, seed0=2)
         line["cpu_baseline"] = {"value": round(r, 3), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                                "sample": f"{len(toks)} seeded tokens of the T={T} batch "
-                                          f"({dt:.1f} s of fp64 CPU work; rows are token-independent)"}
+                                "sample": oracle_sample_note(T, steps) + f" ({sum(times):.1f} s)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     dist_teardown(world)
@@ -589,8 +647,9 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the NVFP4 workload points of the default run")
     ap.add_argument("--workload", default="main", choices=["main", "small"],
                     help="main: the benchmark workload; small: the ncu profiling case")
     ap.add_argument("--config", default=None, choices=list(synth.CONFIGS) + ["deepseek-v3-sweep"],
