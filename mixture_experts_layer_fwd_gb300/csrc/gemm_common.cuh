@@ -73,6 +73,46 @@ DEVINL TileInfo decode_tile(int t, const int* s_prefix, const int* s_off, int GT
   return ti;
 }
 
+struct PairTile {
+  int pb;    // problem: 0 routed, 1 shared
+  int g;     // group inside the problem
+  int row0;  // first row of the tile's tokens in A / C
+  int cnt;   // tokens of the tile (1..TM)
+  int n;     // MMA N: cnt rounded up to 16 (or 32)
+  int blk;   // weight block: 128 features (SwiGLU) or 256 output columns
+};
+
+// Tile t -> (group, weight block, token block) of the CTA-pair kernels
+// (weights on the MMA's M side, tokens on N), token blocks fastest so that
+// the pairs working at the same time share a weight block through L2.  A
+// group of `rows` rows has ceil(rows/TM) token blocks of ng rows each (ng =
+// rows / blocks rounded up to 16, the MMA's N granularity); the last one
+// takes the remainder.
+// NQ: the MMA's N is the block's rows rounded up to a multiple of NQ.
+template <int TM, int NQ = 16>
+DEVINL PairTile decode_pair_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
+  int lo = 0, hi = GT;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  PairTile ti;
+  const bool routed = lo < G;
+  ti.pb = routed ? 0 : 1;
+  ti.g = routed ? lo : 0;
+  const int start = routed ? s_off[lo] : 0;
+  const int rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
+  const int nb = (rows + TM - 1) / TM;
+  const int ng = ((rows + nb - 1) / nb + 15) & ~15;
+  const int local = t - s_prefix[lo];
+  ti.blk = local / nb;
+  const int m = local - ti.blk * nb;
+  ti.row0 = start + m * ng;
+  ti.cnt = min(ng, rows - m * ng);
+  ti.n = (ti.cnt + NQ - 1) & ~(NQ - 1);
+  return ti;
+}
+
 // Loads the group offsets and builds the per-group tile prefix in shared
 // memory.  Called by every thread of the block (contains barriers).
 // Offsets are clamped to [0, rows of A] and a group whose end lies before its
@@ -120,7 +160,33 @@ DEVINL void build_schedule(const Params& p, int* s_off, int* s_prefix, int* warp
   if (threadIdx.x == 0) s_prefix[GT] = warp_sums[NUM_WARPS - 1];
 }
 
-DEVINL float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g * sigmoid(g) with the fast exponential and division (a few ulp;
+// exact zero for g below about -88, where e^-g overflows)
+DEVINL float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// Stores NV tokens x one column per lane as bf16: lanes 2j and 2j+1 hold
+// columns col_even and col_even+1 of the same tokens; after one exchange each
+// lane writes both columns of one token (even lane: tokens 2i, odd lane:
+// tokens 2i+1).  Tokens from valid_tokens on are not stored.
+template <int NV>
+DEVINL void store_pairs(const Prob& P, const float (&h)[NV], int col, int row_first, int valid_tokens, int lane) {
+  const bool odd = lane & 1;
+  const int col_even = col & ~1;
+  if (col_even >= P.n_out) return;  // uniform over the lanes sharing tokens: n_out % 32 == 0
+  uint16_t* C = static_cast<uint16_t*>(P.c);
+#pragma unroll
+  for (int j = 0; j < NV / 2; ++j) {
+    const float send = odd ? h[2 * j] : h[2 * j + 1];
+    const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+    const int t = 2 * j + (odd ? 1 : 0);
+    const float lo = odd ? recv : h[2 * j];
+    const float hi = odd ? h[2 * j + 1] : recv;
+    if (t < valid_tokens)
+      *reinterpret_cast<uint32_t*>(C + static_cast<size_t>(row_first + t) * P.n_out + col_even) =
+          pack_bf16x2(lo, hi);
+  }
+}
+
 
 // Epilogue of one tile held in tensor memory: ACC_N fp32 columns per row.
 // STORE: C[row, n_blk*ACC_N + c] = bf16(scale * acc[c]).

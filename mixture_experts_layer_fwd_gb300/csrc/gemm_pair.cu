@@ -73,65 +73,6 @@ static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
 static_assert(KSUB == 2, "the MMA issuer unrolls two k-blocks per stage");
 static_assert(SMEM <= 232448, "shared memory budget");
 
-struct Tile {
-  int pb;    // problem: 0 routed, 1 shared
-  int g;     // group inside the problem
-  int row0;  // first row of the tile's tokens in A / C
-  int cnt;   // tokens of the tile (1..256)
-  int n;     // MMA N: cnt rounded up to 16
-  int blk;   // weight block: 128 features (SwiGLU) or 256 output columns
-};
-
-// Tile t -> (group, weight block, token block), token blocks fastest so that
-// the pairs working at the same time share a weight block through L2.  A
-// group of `rows` rows has ceil(rows/256) token blocks of ng rows each (ng =
-// rows / blocks rounded up to 16); the last one takes the remainder.
-DEVINL Tile decode_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
-  int lo = 0, hi = GT;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (s_prefix[mid] <= t) lo = mid; else hi = mid;
-  }
-  Tile ti;
-  const bool routed = lo < G;
-  ti.pb = routed ? 0 : 1;
-  ti.g = routed ? lo : 0;
-  const int start = routed ? s_off[lo] : 0;
-  const int rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
-  const int nb = (rows + TM - 1) / TM;
-  const int ng = ((rows + nb - 1) / nb + 15) & ~15;
-  const int local = t - s_prefix[lo];
-  ti.blk = local / nb;
-  const int m = local - ti.blk * nb;
-  ti.row0 = start + m * ng;
-  ti.cnt = min(ng, rows - m * ng);
-  ti.n = (ti.cnt + 15) & ~15;
-  return ti;
-}
-
-// Stores NV tokens x one column per lane as bf16: lanes 2j and 2j+1 hold
-// columns col_even and col_even+1 of the same tokens; after one exchange each
-// lane writes both columns of one token (even lane: tokens 2i, odd lane:
-// tokens 2i+1).  Tokens from valid_tokens on are not stored.
-template <int NV>
-DEVINL void store_pairs(const Prob& P, const float (&h)[NV], int col, int row_first, int valid_tokens, int lane) {
-  const bool odd = lane & 1;
-  const int col_even = col & ~1;
-  if (col_even >= P.n_out) return;  // uniform over the lanes sharing tokens: n_out % 32 == 0
-  uint16_t* C = static_cast<uint16_t*>(P.c);
-#pragma unroll
-  for (int j = 0; j < NV / 2; ++j) {
-    const float send = odd ? h[2 * j] : h[2 * j + 1];
-    const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
-    const int t = 2 * j + (odd ? 1 : 0);
-    const float lo = odd ? recv : h[2 * j];
-    const float hi = odd ? h[2 * j + 1] : recv;
-    if (t < valid_tokens)
-      *reinterpret_cast<uint32_t*>(C + static_cast<size_t>(row_first + t) * P.n_out + col_even) =
-          pack_bf16x2(lo, hi);
-  }
-}
-
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __grid_constant__ Params p) {
   constexpr int S = STAGES;
@@ -200,7 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
       uint32_t phase = 0;
       bool ok = true;
       for (int t = cluster_id; t < total && ok; t += n_clusters) {
-        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const gg::PairTile ti = gg::decode_pair_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
         const Prob& P = p.prob[ti.pb];
         const void* ta = &p.tma_a[ti.pb];
         const void* tw = &p.tma_w[ti.pb];
@@ -246,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
       const uint64_t a_desc0 = smem_desc_kmajor_sw128(smem_u32(stages));
       const uint64_t b_desc0 = smem_desc_kmajor_sw128(smem_u32(stages + KSUB * A_TILE));
       for (int t = cluster_id; t < total && ok; t += n_clusters, ++it) {
-        const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const gg::PairTile ti = gg::decode_pair_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
         const int nk = p.prob[ti.pb].K / BK;
         const uint32_t idesc = idesc_bf16_f32(2 * WM, ti.n);
         const int buf = it & 1;
@@ -309,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
     float* x_to_gate = x_to_up + XCH_FLOATS;     // up values the gate warp consumes
     int it = 0;
     for (int t = cluster_id; t < total; t += n_clusters, ++it) {
-      const Tile ti = decode_tile(t, s_prefix, s_off, GT, G, p.shared_rows);
+      const gg::PairTile ti = gg::decode_pair_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
       const Prob& P = p.prob[ti.pb];
       const int buf = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -348,11 +289,11 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
           if (is_gate) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) h[j] = gg::silu_f(__uint_as_float(v0[j])) * x_to_gate[j * 32 + lane];
-            store_pairs<32>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
+            gg::store_pairs<32>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
           } else if (has1) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) h[j] = gg::silu_f(x_to_up[j * 32 + lane]) * __uint_as_float(v1[j]);
-            store_pairs<32>(P, h, col, ti.row0 + (c + 1) * 32, ti.cnt - (c + 1) * 32, lane);
+            gg::store_pairs<32>(P, h, col, ti.row0 + (c + 1) * 32, ti.cnt - (c + 1) * 32, lane);
           }
           // the slots are rewritten by the next chunk pair
           named_bar_sync(1 + pi, 64);
@@ -366,7 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
           float h[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) h[j] = __uint_as_float(v[j]);
-          store_pairs<32>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
+          gg::store_pairs<32>(P, h, col, ti.row0 + c * 32, ti.cnt - c * 32, lane);
         }
       }
       tc_fence_before();

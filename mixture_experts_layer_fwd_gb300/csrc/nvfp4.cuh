@@ -42,23 +42,57 @@ DEVINL uint32_t e2m1_magnitude(float a) {
          static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) + static_cast<uint32_t>(a > 5.0f);
 }
 
+// A quotient q with the same E2M1 code as the correctly rounded RN(x / d)
+// (d > 0), with one multiply in the common case, given r = RN(1 / d).  The
+// product q = RN(x * r) carries two roundings of at most 2^-24 relative
+// each and RN(x / d) one, so they lie within 4 ulp of q of each other; they
+// can then round to different E2M1 codes only if a decision point of the
+// E2M1 grid (a midpoint between neighbouring magnitudes: 0.25, 0.75, 1.25,
+// 1.75, 2.5, 3.5, 5) lies within those 4 ulp.  Each decision point has at
+// most three significant bits, so its low 21 mantissa bits are zero: when
+// the low 21 mantissa bits of q are more than 8 away from a multiple of
+// 2^21, no decision point is that close and q is returned.  Otherwise (and
+// when q is not finite: d so small that r overflows) the quotient is formed
+// by an IEEE division.
+DEVINL float e2m1_quotient(float x, float d, float r) {
+  const float q = __fmul_rn(x, r);
+  if (((__float_as_uint(q) + 8u) & 0x1FFFFFu) <= 16u || !(fabsf(q) < INFINITY)) return __fdiv_rn(x, d);
+  return q;
+}
+
+// Eight fp32 values -> eight E2M1 codes (element i in nibble i), round to
+// nearest with ties to the even code, saturating to +-6, sign kept (the
+// hardware conversion).
+DEVINL uint32_t e2m1x8_rn_satfinite(const float* v) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
 // Quantise 16 fp32 values with global scale g.  Returns the E4M3 scale byte;
 // codes[0] holds elements 0..7 (element 2j in the low nibble of byte j),
-// codes[1] elements 8..15.
+// codes[1] elements 8..15.  Bit for bit the recipe above with an IEEE
+// division per element (see e2m1_quotient).
 DEVINL uint32_t nvfp4_quantize16(const float (&v)[16], float g, uint32_t (&codes)[2]) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
   const uint32_t s = e4m3_encode_satfinite(__fdiv_rn(amax, __fmul_rn(6.0f, g)));
   const float denom = __fmul_rn(e4m3_decode(s), g);
-  codes[0] = codes[1] = 0u;
+  const float r = denom != 0.0f ? __frcp_rn(denom) : 0.0f;
+  float q[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    uint32_t mag = 0u;
-    if (denom != 0.0f) mag = e2m1_magnitude(fabsf(__fdiv_rn(v[i], denom)));
-    const uint32_t code = mag | ((__float_as_uint(v[i]) >> 31) << 3);
-    codes[i >> 3] |= code << (4 * (i & 7));
-  }
+  for (int i = 0; i < 16; ++i)
+    q[i] = denom != 0.0f ? e2m1_quotient(v[i], denom, r) : copysignf(0.0f, v[i]);  // magnitude 0 if denom == 0
+  codes[0] = e2m1x8_rn_satfinite(q);
+  codes[1] = e2m1x8_rn_satfinite(q + 8);
   return s;
 }
 

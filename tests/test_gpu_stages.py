@@ -468,3 +468,47 @@ def test_grouped_gemm_nvfp4_both_with_nvfp4_output():
     assert np.mean(nvfp4.unpack_codes(got_q) != nvfp4.unpack_codes(rq)) < 2e-3
     err = oracle.rel_frobenius(nvfp4.dequantize(got_q, got_s, gh), nvfp4.dequantize(rq, rs, gh))
     assert err < 1e-2, err
+
+
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_grouped_gemm_nvfp4_both_many_row_blocks(epi):
+    """NVFP4 x NVFP4 with groups that span several row tiles (161, 320, 321,
+    1000 rows), tiles far from full (1, 17, 31, 33 rows), 159/160-row groups
+    and an empty one; every epilogue, weight tiles past N (N = 448 STORE,
+    320 features SwiGLU), K = 1536."""
+    m = api()
+    counts = [161, 320, 1, 17, 0, 321, 31, 1000, 33, 159, 160]
+    offs = _ragged_offsets(counts)
+    M, G, K = int(offs[-1]), len(counts), 1536
+    N = 448 if epi == 0 else 320
+    Wn = N if epi == 0 else 2 * N
+    g = torch.Generator().manual_seed(40 + epi)
+    Aq, As, Ag = nvfp4.quantize(torch.randn(M, K, generator=g).numpy())
+    Wq = [nvfp4.quantize((torch.randn(Wn, K, generator=g) * 0.02).numpy()) for _ in range(G)]
+    gh = F32(8.0 / 2688)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    out = m.moe_grouped_gemm(1, 1, epi, offs.to(DEV), N, K, t(Aq), t(np.stack([q for q, _, _ in Wq])), A_sf=t(As),
+                             A_g=torch.tensor([Ag], device=DEV), W_sf=t(np.stack([s for _, s, _ in Wq])),
+                             W_g=torch.tensor([gg for _, _, gg in Wq], dtype=torch.float32, device=DEV),
+                             c_g=torch.tensor([gh], device=DEV) if epi == 2 else None)
+    _sync()
+    Ad = nvfp4.dequantize(Aq, As, Ag)
+    Wd = np.stack([nvfp4.dequantize(q, s, gg) for q, s, gg in Wq])
+    ref = _gemm_ref(Ad, Wd, offs.numpy(), epi != 0, N)
+    if epi == 2:
+        C, C_sf = out
+        rq, rs, _ = nvfp4.quantize(ref.astype(F32), gh)
+        got_q, got_s = C.cpu().numpy(), C_sf.cpu().numpy()
+        assert np.mean(got_s != rs) < 1e-3
+        assert np.mean(nvfp4.unpack_codes(got_q) != nvfp4.unpack_codes(rq)) < 2e-3
+        got = nvfp4.dequantize(got_q, got_s, gh)
+        ref = nvfp4.dequantize(rq, rs, gh)
+        tol = 1e-2
+    else:
+        got = out.float().cpu().numpy()
+        tol = 5e-3
+    err = oracle.rel_frobenius(got, ref)
+    assert err < tol, err
+    # every row is written: no row keeps the allocation's contents
+    row_err = np.abs(got - ref).max(axis=1) / (np.abs(ref).max() + 1e-30)
+    assert row_err.max() < 5e-2, int(row_err.argmax())
