@@ -379,11 +379,12 @@ def run_reference(args):
 # DeepSeek-V3-shaped layer (NVFP4 weights and activations).
 EXTRA_POINTS = (("qwen35-397b", (64, 512, 4096)), ("deepseek-v3", (256, 16384)))
 EXTRA_STEPS = 20
-STAGES = ["route", "quant", "permute", "gemm_gate_up", "gemm_down", "combine"]
+STAGES = ["quant", "dispatch", "gemm_gate_up", "gemm_down", "combine"]
+N_EVENTS = len(STAGES) + 1
 
 
 def new_events():
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(N_EVENTS)]
     for ev in evs:
         ev.record()  # creates the underlying CUDA events
     return evs
@@ -406,7 +407,7 @@ def timed_steps(api, layer, x, logits, out, ws, flush, steps, warmup, evsets=Non
 
 
 def stage_table(evsets):
-    return np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(6)] for evs in evsets])
+    return np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(len(STAGES))] for evs in evsets])
 
 
 def active_experts(api, logits, cfg):
@@ -425,8 +426,8 @@ def measure_point(api, moe_sync_status, layer, cfg, T, dev, flush, steps, warmup
     if moe_sync_status() != 0:
         raise RuntimeError(f"device status not clean at {cfg.name} T={T}")
     st = stage_table(evsets)
-    ms = float(np.mean([evs[0].elapsed_time(evs[6]) for evs in evsets]))
-    gemm_ms = float(np.mean(st[:, 3] + st[:, 4]))
+    ms = float(np.mean([evs[0].elapsed_time(evs[-1]) for evs in evsets]))
+    gemm_ms = float(np.mean(st[:, 2] + st[:, 3]))
     active = active_experts(api, logits, cfg)
     return {"ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "active_experts": active,
             "roofline": roofline(cfg, T, gemm_ms, active, None, src),
@@ -488,14 +489,14 @@ def run_gpu(args):
             # bracket it (stage times come from the profiled warm-up below)
             evsets[i][0].record()
             graph.launch()
-            evsets[i][6].record()
+            evsets[i][-1].record()
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
     if moe_sync_status() != 0:
         raise RuntimeError("device status not clean after the timed steps")
 
-    step_ms = [evs[0].elapsed_time(evs[6]) for evs in evsets]
+    step_ms = [evs[0].elapsed_time(evs[-1]) for evs in evsets]
     if graph is not None:
         # per-stage times of the same forward, launched stage by stage
         timed_steps(api, layer, x, logits, out, ws, flush, args.steps, 0, evsets)
@@ -504,7 +505,7 @@ def run_gpu(args):
     total_ms = total_s * 1e3
 
     active = active_experts(api, logits, cfg)
-    gemm_ms = float(np.mean(stage_ms[:, 3] + stage_ms[:, 4]))
+    gemm_ms = float(np.mean(stage_ms[:, 2] + stage_ms[:, 3]))
     _, src = peaks()
     roof = roofline(cfg, T, gemm_ms, active, gemm_traffic_per_launch() if is_main else None, src)
 
@@ -526,7 +527,10 @@ def run_gpu(args):
     e2e_value, _ = job_rate(T, float(np.mean(e2e_t)), world, dev)
 
     a4 = cfg.act_fmt == "nvfp4"
-    launches = 8 + (2 if a4 else 0)  # route, 4 permute, 2 GEMM, combine (+ amax, quantise)
+    # dispatch: one fused route + permutation kernel at T*k <= 4096 (its
+    # barrier-counter memset is not a kernel), else route + 4 permutation
+    # kernels; 2 grouped GEMMs; combine; + amax and quantise on NVFP4 activations
+    launches = (1 if T * cfg.k <= 4096 else 5) + 3 + (2 if a4 else 0)
     line = {
         "metric": metric_name(cfg, T), "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
@@ -613,7 +617,7 @@ def run_sweep(args):
             x_full, lg_full = acts.x.to(dev), acts.logits.to(dev)
             for T in Ts:
                 x, lg, out = x_full[:T].contiguous(), lg_full[:T].contiguous(), out_full[:T]
-                evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(N_EVENTS)]
                 for ev in evs:
                     ev.record()
                 steps = args.sweep_steps
@@ -623,7 +627,7 @@ def run_sweep(args):
                     api.moe_forward_profiled(layer.c, x, lg, out, ws, evs)
                     torch.cuda.synchronize()
                     if i >= args.warmup:
-                        res.append((evs[0].elapsed_time(evs[6]), evs[3].elapsed_time(evs[5])))
+                        res.append((evs[0].elapsed_time(evs[-1]), evs[2].elapsed_time(evs[4])))
                 if moe_sync_status() != 0:
                     raise RuntimeError(f"device status not clean at {fmt} z={z} T={T}")
                 idx, _ = api.moe_route(lg, cfg.k)

@@ -203,6 +203,39 @@ int moe_permute_noalloc(const int32_t* idx, int T, int k, int E,
                         int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
                         void* xp_rows, uint8_t* xp_sf, void* stream);
 
+/* ----------------------------------------------------------- route_permute
+ * Fused dispatch: moe_route_ex followed by moe_permute in one cooperative
+ * launch of at most min(T, SMs, 256) blocks, joined by two grid barriers
+ * ("CuTeDSL at Perplexity", local dispatch, decode variant: routing inside
+ * the dispatch kernel, which signals the rest of the grid and hands out
+ * slots from shared-memory counters; grid-sync section: a grid barrier costs
+ * about 3 us against a second launch; "Como Servimos um Modelo MoE de
+ * 397B ...", section "Roadmap restante": fuse the top-k selection).
+ * Results (idx, w, counts, offsets, row_of, src_tok, permuted rows and
+ * scales) are those of the two calls, bit for bit; arguments as there.
+ * Each grid-barrier wait is bounded in time (moe_set_wait_timeout_ns); a
+ * wait that runs out records MOE_ERR_TIMEOUT (moe_sync_status) and the
+ * kernel returns with the outputs unspecified.  The workspace holds the
+ * per-block histograms and the barrier counter, which a memset on `stream`
+ * zeroes before the launch.
+ * Limits: 1 <= k <= min(E, 32), E <= 1024, T*k < 2^27.  Workspace:
+ * moe_route_permute_workspace_size(T, k, E). */
+size_t moe_route_permute_workspace_size(int T, int k, int E);
+int moe_route_permute(const float* logits, int T, int E, int k, int renorm,
+                      int32_t* idx, float* w,
+                      const void* x_rows, int row_bytes,
+                      const uint8_t* x_sf, int sf_row_bytes,
+                      int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
+                      void* xp_rows, uint8_t* xp_sf,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Test hook for the grid barrier's time-out: a cooperative launch of two
+ * blocks waits for a third arrival that never comes; each wait gives up
+ * after `timeout_ns`, records MOE_ERR_TIMEOUT in the device error word and
+ * the kernel returns; the context stays usable.  Read the result with
+ * moe_sync_status(). */
+int moe_selftest_grid_barrier_timeout(unsigned long long timeout_ns, void* stream);
+
 /* ------------------------------------------------------------ quant_nvfp4
  * NVFP4 quantisation of bf16 matrices (activations before dispatch:
  * "Driving vLLM WideEP ... (Part I)", section "NVFP4 MoE dispatch"; abs-max
@@ -366,9 +399,11 @@ typedef struct {
  * a T that moe_forward rejects). */
 size_t moe_forward_workspace_size(const moe_layer* L, int T);
 
-/* The whole layer: route -> (NVFP4 activation quantisation) -> permute ->
- * grouped GEMM gate/up + SwiGLU -> grouped GEMM down -> combine, with the
- * shared expert folded into both grouped GEMM launches.
+/* The whole layer: (NVFP4 / MX activation quantisation) -> router top-k and
+ * permutation (one launch as in moe_route_permute when T*k <= 4096, else
+ * moe_route_ex and moe_permute) -> grouped GEMM gate/up +
+ * SwiGLU -> grouped GEMM down -> combine, with the shared expert folded into
+ * both grouped GEMM launches.
  *   x      : bf16 [T, H]
  *   logits : fp32 [T, E]
  *   out    : bf16 [T, H]
@@ -379,11 +414,13 @@ int moe_forward(const moe_layer* L, const uint16_t* x, const float* logits, int 
 
 /* moe_forward that also records caller-created CUDA events (cudaEvent_t
  * passed as void*) on `stream` at the stage boundaries, for live per-stage
- * timing: events[0] before routing, [1] after routing, [2] after the NVFP4
- * activation quantisation (nothing is launched there on bf16 activations),
- * [3] after the permutation, [4] after the gate/up grouped GEMM, [5] after
- * the down grouped GEMM, [6] after the combine.  `events` may be NULL, and
- * any entry may be NULL to skip it.  Launches exactly the kernels of
+ * timing: events[0] before the first launch, [1] after the activation
+ * quantisation and the shared-expert gate (nothing is launched there on
+ * plain bf16 layers), [2] after the router top-k and the permutation (one
+ * fused launch as in moe_route_permute when T*k <= 4096, else the router and
+ * permutation kernels), [3] after the gate/up grouped GEMM, [4]
+ * after the down grouped GEMM, [5] after the combine.  `events` may be NULL,
+ * and any entry may be NULL to skip it.  Launches exactly the kernels of
  * moe_forward. */
 int moe_forward_profiled(const moe_layer* L, const uint16_t* x, const float* logits, int T,
                          uint16_t* out, void* ws, size_t ws_bytes, void* const* events,

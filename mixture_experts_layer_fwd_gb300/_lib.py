@@ -62,6 +62,12 @@ SIGNATURES = {
                             c_void_p, c_size_t, c_void_p]),
     "moe_permute_noalloc": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_int, c_void_p, c_int,
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "moe_route_permute_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "moe_route_permute": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                                  c_void_p, c_int, c_void_p, c_int,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_size_t, c_void_p]),
+    "moe_selftest_grid_barrier_timeout": (c_int, [c_ull, c_void_p]),
     "moe_quant_nvfp4_workspace_size": (c_size_t, [c_int]),
     "moe_quant_nvfp4": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),

@@ -191,6 +191,49 @@ def moe_permute_noalloc(idx: torch.Tensor, E: int, x_rows: Optional[torch.Tensor
     return o
 
 
+def moe_route_permute(logits: torch.Tensor, k: int, x_rows: Optional[torch.Tensor] = None,
+                      x_sf: Optional[torch.Tensor] = None, renorm: bool = True, stream=None):
+    """Fused dispatch: moe_route then moe_permute in one cooperative launch.
+    logits fp32 [T, E]; x_rows / x_sf as for moe_permute.  Returns dict(idx,
+    w, counts, offsets, row_of, src_tok, xp, xp_sf)."""
+    _dev(logits, "logits", dtype=torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits: expected [T, E]")
+    T, E = logits.shape
+    dev = logits.device
+    o = dict(idx=torch.empty(T, k, dtype=torch.int32, device=dev), w=torch.empty(T, k, device=dev),
+             counts=torch.empty(E, dtype=torch.int32, device=dev),
+             offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+             row_of=torch.empty(T, k, dtype=torch.int32, device=dev),
+             src_tok=torch.empty(T * k, dtype=torch.int32, device=dev), xp=None, xp_sf=None)
+    row_bytes = sf_bytes = 0
+    if x_rows is not None:
+        _dev(x_rows, "x_rows", device=dev)
+        if x_rows.shape[0] != T:
+            raise ValueError("x_rows: expected one row per token")
+        row_bytes = x_rows[0].numel() * x_rows.element_size() if T else 0
+        o["xp"] = torch.empty((T * k,) + tuple(x_rows.shape[1:]), dtype=x_rows.dtype, device=dev)
+        if x_sf is not None:
+            _dev(x_sf, "x_sf", dtype=torch.uint8, device=dev)
+            if x_sf.dim() != 2 or x_sf.shape[0] != T:
+                raise ValueError("x_sf: expected [T, sf_bytes]")
+            sf_bytes = x_sf.shape[1]
+            o["xp_sf"] = torch.empty(T * k, sf_bytes, dtype=torch.uint8, device=dev)
+    lib = load()
+    nbytes = lib.moe_route_permute_workspace_size(T, k, E)
+    ws = _ws(nbytes, dev)
+    check(lib.moe_route_permute(_ptr(logits), T, E, k, 1 if renorm else 0, _ptr(o["idx"]), _ptr(o["w"]),
+                                _ptr(x_rows), row_bytes, _ptr(x_sf), sf_bytes, _ptr(o["counts"]),
+                                _ptr(o["offsets"]), _ptr(o["row_of"]), _ptr(o["src_tok"]), _ptr(o["xp"]),
+                                _ptr(o["xp_sf"]), _ptr(ws), nbytes, _stream(stream)), "moe_route_permute")
+    return o
+
+
+def moe_selftest_grid_barrier_timeout(timeout_ns: int, stream=None) -> None:
+    check(load().moe_selftest_grid_barrier_timeout(int(timeout_ns), _stream(stream)),
+          "moe_selftest_grid_barrier_timeout")
+
+
 def moe_quant_nvfp4(x: torch.Tensor, g_in: Optional[torch.Tensor] = None, stream=None):
     """x bf16 [rows, cols] or [groups, rows, cols] -> (codes uint8 [..., cols/2],
     sf uint8 [..., cols/16], g fp32 [groups])."""
@@ -373,13 +416,15 @@ def moe_forward(layer_c, x: torch.Tensor, logits: torch.Tensor, out: torch.Tenso
 
 def moe_forward_profiled(layer_c, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
                          events, stream=None) -> torch.Tensor:
-    """moe_forward recording 7 torch.cuda.Event objects at the stage
-    boundaries (see include/moe_gb300.h)."""
+    """moe_forward recording 6 torch.cuda.Event objects at the stage
+    boundaries: start, after the activation quantisation, after the router
+    top-k and permutation, after each grouped GEMM, after the combine (see
+    include/moe_gb300.h)."""
     import ctypes
-    if len(events) != 7:
-        raise ValueError("events: expected 7 torch.cuda.Event objects")
+    if len(events) != 6:
+        raise ValueError("events: expected 6 torch.cuda.Event objects")
     T = _forward_args(layer_c, x, logits, out, ws)
-    handles = (ctypes.c_void_p * 7)(*[ev.cuda_event for ev in events])
+    handles = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events])
     check(load().moe_forward_profiled(ctypes.byref(layer_c), _ptr(x), _ptr(logits), T, _ptr(out), _ptr(ws),
                                       ws.numel(), handles, _stream(stream)), "moe_forward_profiled")
     return out
@@ -401,7 +446,8 @@ def moe_forward_host(layer_c, x_host: torch.Tensor, logits_host: torch.Tensor, o
 
 __all__ = ["MOE_FMT_BF16", "MOE_FMT_NVFP4", "MOE_FMT_MXFP8", "MOE_FMT_MXFP4", "moe_quant_mx", "MOE_EPI_STORE_BF16", "MOE_EPI_SWIGLU_BF16",
            "MOE_EPI_SWIGLU_NVFP4", "moe_version", "moe_sync_status", "moe_set_wait_timeout_ns",
-           "moe_selftest_wait_timeout", "moe_route", "moe_permute", "moe_quant_nvfp4",
+           "moe_selftest_wait_timeout", "moe_selftest_grid_barrier_timeout", "moe_route", "moe_permute",
+           "moe_route_permute", "moe_quant_nvfp4", "MOE_EPI_SWIGLU_MX",
            "moe_permute_noalloc", "moe_grouped_gemm", "moe_combine", "moe_shared_gate",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_profiled", "moe_forward_host",
            "ForwardGraph"]

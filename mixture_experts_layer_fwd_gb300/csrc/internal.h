@@ -13,6 +13,14 @@ int permute_launch(const int32_t* idx, int T, int k, int E, const void* x_rows, 
                    int sf_row_bytes, int32_t* counts, int32_t* offsets, int32_t* row_of, int32_t* src_tok,
                    void* xp_rows, uint8_t* xp_sf, void* ws, size_t ws_bytes, cudaStream_t s, bool to_f16 = false);
 
+// Fused router + permutation in one cooperative launch (dispatch.cu); the
+// same results as moe_route_ex followed by permute_launch.  E <= 1024.
+size_t route_permute_ws_bytes(int T, int E);
+int route_permute_launch(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
+                         const void* x_rows, int row_bytes, const uint8_t* x_sf, int sf_row_bytes, int32_t* counts,
+                         int32_t* offsets, int32_t* row_of, int32_t* src_tok, void* xp_rows, uint8_t* xp_sf,
+                         void* ws, size_t ws_bytes, cudaStream_t s, bool to_f16 = false);
+
 size_t quant_ws_bytes(int groups);
 int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float* g_in, uint8_t* codes, uint8_t* sf,
                  float* g_out, void* ws, size_t ws_bytes, cudaStream_t s);

@@ -24,6 +24,7 @@
 // counted, row_of = -1, no permuted row), the device error word records
 // kErrBadIndex, and no kernel touches memory outside its buffers.
 #include "internal.h"
+#include "permute.cuh"
 
 namespace moe {
 
@@ -153,22 +154,9 @@ __global__ void __launch_bounds__(32) permute_assign_kernel(const int32_t* __res
   }
 }
 
-DEVINL uint32_t bf16x2_to_f16x2_satfinite(uint32_t v) {
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(v & 0xFFFF0000u)),
-      "f"(__uint_as_float(v << 16)));
-  return r;
-}
-DEVINL uint4 cvt_row_vec(uint4 v, bool to_f16) {
-  if (!to_f16) return v;
-  return make_uint4(bf16x2_to_f16x2_satfinite(v.x), bf16x2_to_f16x2_satfinite(v.y), bf16x2_to_f16x2_satfinite(v.z),
-                    bf16x2_to_f16x2_satfinite(v.w));
-}
-
-// One warp per permuted row; copies row_bytes (multiple of 16) and sf bytes
-// (multiple of 4).  to_f16: the row holds bf16 values, written as fp16.
-// Rows past offsets[E] exist only when slots were left out; their src_tok
-// entries were never written, so a token id outside [0, T) is skipped.
+// One warp per permuted row (copy_row, permute.cuh).  Rows past offsets[E]
+// exist only when slots were left out; their src_tok entries were never
+// written, so a token id outside [0, T) is skipped.
 template <bool TO_F16>
 __global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __restrict__ src_tok, int S, int T,
                                                              const uint8_t* __restrict__ x, int row_bytes,
@@ -179,23 +167,7 @@ __global__ void __launch_bounds__(256) permute_gather_kernel(const int32_t* __re
   if (r >= S) return;
   const int t = __ldg(src_tok + r);
   if (static_cast<unsigned>(t) >= static_cast<unsigned>(T)) return;
-  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * row_bytes);
-  uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(r) * row_bytes);
-  const int nvec = row_bytes >> 4;
-  int i = lane;
-  for (; i + 96 < nvec; i += 128) {
-    const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
-    dst[i] = cvt_row_vec(a, TO_F16);
-    dst[i + 32] = cvt_row_vec(b, TO_F16);
-    dst[i + 64] = cvt_row_vec(c, TO_F16);
-    dst[i + 96] = cvt_row_vec(d, TO_F16);
-  }
-  for (; i < nvec; i += 32) dst[i] = cvt_row_vec(__ldg(src + i), TO_F16);
-  if (x_sf != nullptr) {
-    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(x_sf + static_cast<size_t>(t) * sf_bytes);
-    uint32_t* sdst = reinterpret_cast<uint32_t*>(xp_sf + static_cast<size_t>(r) * sf_bytes);
-    for (int j = lane; j < (sf_bytes >> 2); j += 32) sdst[j] = __ldg(ssrc + j);
-  }
+  copy_row<TO_F16>(x, row_bytes, x_sf, sf_bytes, t, xp, xp_sf, r, lane);
 }
 
 size_t permute_ws_bytes(int T, int k, int E) {

@@ -44,14 +44,14 @@ def test_layer_calls_reject_host_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         m.moe_forward(c, x, logits, out, ws)
     with pytest.raises(ValueError, match="CUDA"):
-        m.moe_forward_profiled(c, x, logits, out, ws, [None] * 7)
+        m.moe_forward_profiled(c, x, logits, out, ws, [None] * 6)
     with pytest.raises(ValueError, match="CUDA"):
         # the device-side buffers of the host entry point must be on a GPU
         m.moe_forward_host(c, x, logits, out, x, logits, out, ws)
     with pytest.raises(ValueError, match="CUDA"):
         m.api.ForwardGraph(c, x, logits, out, ws)  # and its destructor has nothing to free
-    with pytest.raises(ValueError, match="7"):
-        m.moe_forward_profiled(c, x, logits, out, ws, [None] * 6)
+    with pytest.raises(ValueError, match="6"):
+        m.moe_forward_profiled(c, x, logits, out, ws, [None] * 7)
 
 
 def test_layer_rejects_host_weights_and_unknown_formats():

@@ -45,6 +45,19 @@ def test_bounded_wait_times_out_and_context_survives():
     assert idx.shape == (4, 2)
 
 
+def test_grid_barrier_times_out_and_context_survives():
+    """The fused dispatch's grid barrier: a wait for an arrival that never
+    comes gives up after its limit, records MOE_ERR_TIMEOUT, and the kernel
+    returns; the context stays usable."""
+    m = api()
+    m.moe_selftest_grid_barrier_timeout(2_000_000)  # 2 ms
+    assert m.moe_sync_status() == 5                 # MOE_ERR_TIMEOUT
+    assert m.moe_sync_status() == 0
+    r = m.moe_route_permute(torch.randn(16, 8, device=DEV), 2)
+    _sync()
+    assert int(r["offsets"][-1]) == 32
+
+
 # ------------------------------------------------------------------ route ----
 def _check_route(logits: torch.Tensor, k: int):
     idx, w = api().moe_route(logits.to(DEV).contiguous(), k)
@@ -134,6 +147,62 @@ def test_permute_zero_tokens():
     r = api().moe_permute(torch.empty(0, 4, dtype=torch.int32, device=DEV), 16)
     _sync()
     assert r["counts"].cpu().tolist() == [0] * 16 and r["offsets"].cpu().tolist() == [0] * 17
+
+
+# ---------------------------------------------------------- fused dispatch ----
+@pytest.mark.parametrize("name,T", [("tiny", 64), ("qwen3-235b", 256), ("qwen3-235b", 16), ("qwen35-397b", 64),
+                                    ("qwen35-397b", 512), ("deepseek-v3", 256), ("deepseek-v3", 16384),
+                                    ("qwen3-235b", 8192), ("tiny", 1), ("tiny", 153)])
+def test_route_permute_matches_oracle_and_split_calls(name, T):
+    """moe_route_permute (route + permutation in one cooperative launch) at
+    the workloads' decode and prefill sizes: idx bit-exact and w within 1e-6
+    of the oracle's router; counts, offsets, row_of, src_tok and the
+    permuted rows bit-exact with the oracle's permutation; every output
+    bit-exact with moe_route followed by moe_permute."""
+    m = api()
+    cfg = synth.CONFIGS[name]
+    acts = synth.make_activations(cfg, T, seed=T)
+    lg = acts.logits.to(DEV)
+    x = acts.x.to(DEV)
+    r = m.moe_route_permute(lg, cfg.k, x)
+    _sync()
+    ridx, rw = oracle.route(acts.logits.numpy(), cfg.k)
+    assert np.array_equal(r["idx"].cpu().numpy(), ridx)
+    np.testing.assert_allclose(r["w"].cpu().numpy().astype(np.float64), rw, rtol=1e-6, atol=0)
+    p = oracle.permute(ridx, cfg.E)
+    for key, ref in (("counts", p.counts), ("offsets", p.offsets), ("row_of", p.row_of), ("src_tok", p.src_tok)):
+        assert np.array_equal(r[key].cpu().numpy(), ref), key
+    assert torch.equal(r["xp"].cpu().view(torch.int16), acts.x[torch.from_numpy(p.src_tok).long()].view(torch.int16))
+    idx, w = m.moe_route(lg, cfg.k)
+    q = m.moe_permute(idx, cfg.E, x)
+    _sync()
+    assert torch.equal(r["idx"], idx) and torch.equal(r["w"], w)
+    for key in ("counts", "offsets", "row_of", "src_tok", "xp"):
+        assert torch.equal(r[key], q[key]), key
+
+
+def test_route_permute_nvfp4_rows_scales_and_variants():
+    """Packed rows with scale bytes, the router without renormalisation, hot
+    experts that leave others empty, E = 1024 (the router's limit)."""
+    m = api()
+    for T, E, k, renorm in ((3000, 64, 4, True), (700, 1024, 8, False), (5, 16, 16, True)):
+        g = torch.Generator().manual_seed(T)
+        rank = torch.randperm(E, generator=g).double() + 1
+        logits = (torch.randn(T, E, generator=g, dtype=torch.float64) - 2.0 * torch.log(rank)).float()
+        rows = torch.randint(0, 256, (T, 256), generator=g, dtype=torch.uint8)
+        sf = torch.randint(0, 256, (T, 32), generator=g, dtype=torch.uint8)
+        r = m.moe_route_permute(logits.to(DEV), k, rows.to(DEV), sf.to(DEV), renorm=renorm)
+        _sync()
+        ridx, rw = oracle.route(logits.numpy(), k, renorm=renorm)
+        assert np.array_equal(r["idx"].cpu().numpy(), ridx)
+        np.testing.assert_allclose(r["w"].cpu().numpy().astype(np.float64), rw, rtol=1e-6, atol=0)
+        p = oracle.permute(ridx, E)
+        assert np.array_equal(r["offsets"].cpu().numpy(), p.offsets)
+        assert np.array_equal(r["row_of"].cpu().numpy(), p.row_of)
+        src = torch.from_numpy(p.src_tok).long()
+        assert torch.equal(r["xp"].cpu(), rows[src]) and torch.equal(r["xp_sf"].cpu(), sf[src])
+        if E == 64:
+            assert (p.counts == 0).any()
 
 
 # ----------------------------------------------------------------- quant ----
