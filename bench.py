@@ -527,10 +527,9 @@ def run_gpu(args):
     e2e_value, _ = job_rate(T, float(np.mean(e2e_t)), world, dev)
 
     a4 = cfg.act_fmt == "nvfp4"
-    # dispatch: one fused route + permutation kernel at T*k <= 4096 (its
-    # barrier-counter memset is not a kernel), else route + 4 permutation
-    # kernels; 2 grouped GEMMs; combine; + amax and quantise on NVFP4 activations
-    launches = (1 if T * cfg.k <= 4096 else 5) + 3 + (2 if a4 else 0)
+    # fused route + permutation (its barrier-counter memset is not a kernel),
+    # 2 grouped GEMMs, combine (+ amax and quantise on NVFP4 activations)
+    launches = 4 + (2 if a4 else 0)
     line = {
         "metric": metric_name(cfg, T), "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),

@@ -205,7 +205,8 @@ int moe_permute_noalloc(const int32_t* idx, int T, int k, int E,
 
 /* ----------------------------------------------------------- route_permute
  * Fused dispatch: moe_route_ex followed by moe_permute in one cooperative
- * launch of at most min(T, SMs, 256) blocks, joined by two grid barriers
+ * launch of min(T, SMs, 256) blocks of 1024 threads, joined by two grid
+ * barriers
  * ("CuTeDSL at Perplexity", local dispatch, decode variant: routing inside
  * the dispatch kernel, which signals the rest of the grid and hands out
  * slots from shared-memory counters; grid-sync section: a grid barrier costs
@@ -400,8 +401,7 @@ typedef struct {
 size_t moe_forward_workspace_size(const moe_layer* L, int T);
 
 /* The whole layer: (NVFP4 / MX activation quantisation) -> router top-k and
- * permutation (one launch as in moe_route_permute when T*k <= 4096, else
- * moe_route_ex and moe_permute) -> grouped GEMM gate/up +
+ * permutation in one launch (as moe_route_permute) -> grouped GEMM gate/up +
  * SwiGLU -> grouped GEMM down -> combine, with the shared expert folded into
  * both grouped GEMM launches.
  *   x      : bf16 [T, H]
@@ -417,8 +417,7 @@ int moe_forward(const moe_layer* L, const uint16_t* x, const float* logits, int 
  * timing: events[0] before the first launch, [1] after the activation
  * quantisation and the shared-expert gate (nothing is launched there on
  * plain bf16 layers), [2] after the router top-k and the permutation (one
- * fused launch as in moe_route_permute when T*k <= 4096, else the router and
- * permutation kernels), [3] after the gate/up grouped GEMM, [4]
+ * fused launch, as moe_route_permute), [3] after the gate/up grouped GEMM, [4]
  * after the down grouped GEMM, [5] after the combine.  `events` may be NULL,
  * and any entry may be NULL to skip it.  Launches exactly the kernels of
  * moe_forward. */

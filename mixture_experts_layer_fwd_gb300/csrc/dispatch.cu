@@ -38,8 +38,9 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 1024;  // 32 warps: enough row copies in flight per SM to stream at HBM speed
 constexpr int kWarps = kThreads / 32;
+constexpr int kScanPer = (1024 + kThreads - 1) / kThreads;  // experts per thread in the offsets scan
 constexpr int kMaxBlocks = 256;  // grid of the fused dispatch: one block per SM, at most this many
 
 struct DispatchArgs {
@@ -121,25 +122,31 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(const DispatchA
   for (int e = threadIdx.x; e < E; e += kThreads) a.hist[static_cast<size_t>(b) * E + e] = sh[e];
   if (!grid_barrier(a.bar, static_cast<unsigned int>(nb), a.timeout_ns, a.err, &s_ok)) return;
 
-  // ---- phase B: per-expert column scans over the blocks
+  // ---- phase B: per-expert column scans over the blocks, the per-block
+  // counts read 8 at a time so that the loads overlap
   for (int e = b * kThreads + threadIdx.x; e < E; e += nb * kThreads) {
     int run = 0;
-    for (int c = 0; c < nb; ++c) {
-      const int h = __ldcg(a.hist + static_cast<size_t>(c) * E + e);
-      a.base[static_cast<size_t>(c) * E + e] = run;
-      run += h;
+    for (int c0 = 0; c0 < nb; c0 += 8) {
+      int h8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) h8[u] = c0 + u < nb ? __ldcg(a.hist + static_cast<size_t>(c0 + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < nb) a.base[static_cast<size_t>(c0 + u) * E + e] = run;
+        run += h8[u];
+      }
     }
     a.counts[e] = run;
   }
   if (!grid_barrier(a.bar, 2u * static_cast<unsigned int>(nb), a.timeout_ns, a.err, &s_ok)) return;
 
-  // ---- phase C: offsets (exclusive scan of counts, E <= 1024: four per
-  // thread), this block's starting positions, slot assignment, row copies
-  int c4[4];
+  // ---- phase C: offsets (exclusive scan of counts, E <= 1024: kScanPer
+  // per thread), this block's starting positions, slot assignment, row copies
+  int c4[kScanPer];
   int loc = 0;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = threadIdx.x * 4 + u;
+  for (int u = 0; u < kScanPer; ++u) {
+    const int e = threadIdx.x * kScanPer + u;
     c4[u] = e < E ? __ldcg(a.counts + e) : 0;
     loc += c4[u];
   }
@@ -154,8 +161,8 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(const DispatchA
   int run = incl - loc;
   for (int i = 0; i < warp; ++i) run += warp_tot[i];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = threadIdx.x * 4 + u;
+  for (int u = 0; u < kScanPer; ++u) {
+    const int e = threadIdx.x * kScanPer + u;
     if (e < E) {
       sh[e] = run + __ldcg(a.base + static_cast<size_t>(b) * E + e);
       if (b == 0) a.offsets[e] = run;

@@ -1,6 +1,5 @@
 // The whole layer: (NVFP4 / MX activation quantisation) -> router top-k and
-// permutation (one cooperative launch at decode sizes, dispatch.cu; the
-// router and permutation kernels otherwise) -> grouped GEMM gate/up +
+// permutation (one cooperative launch, dispatch.cu) -> grouped GEMM gate/up +
 // SwiGLU -> grouped GEMM down -> combine, all stream-ordered on the caller's
 // stream with no host synchronisation.
 //
@@ -12,9 +11,6 @@
 // dispatch").  The shared expert is folded into both grouped GEMM launches
 // as one more group over all T tokens.
 #include "internal.h"
-
-extern "C" int moe_route_ex(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
-                            void* stream);
 
 namespace moe {
 namespace {
@@ -45,22 +41,14 @@ struct FwdBufs {
 
 inline bool is_mx(int fmt) { return fmt == MOE_FMT_MXFP4 || fmt == MOE_FMT_MXFP8; }
 
-// Decode-sized batches take the fused dispatch (router + permutation in one
-// cooperative launch, dispatch.cu); larger ones the split kernels, whose
-// row copy spreads over more warps per SM (measured on GB300: fused 0.027 vs
-// 0.038 ms at 640 routed slots, equal near 5120, 0.29 vs 0.18 ms at 65536).
-constexpr long long kFusedDispatchMaxSlots = 4096;
-
-// Router top-k and permutation of the layer's rows (x_rows: bf16 or coded
-// rows of row_bytes, with optional scale bytes).
+// Router top-k and permutation of the layer's rows in one cooperative launch
+// (dispatch.cu; measured faster than the router + permutation kernels at
+// every size of the workloads here).  x_rows: bf16 or coded rows of
+// row_bytes, with optional scale bytes.
 int dispatch(const float* logits, int T, int E, int k, int renorm, const FwdBufs& b, const void* x_rows,
              int row_bytes, const uint8_t* x_sf, int sf_bytes, cudaStream_t s, bool to_f16 = false) {
-  if (static_cast<long long>(T) * k <= kFusedDispatchMaxSlots)
-    return route_permute_launch(logits, T, E, k, renorm, b.idx, b.w, x_rows, row_bytes, x_sf, sf_bytes, b.counts,
-                                b.offsets, b.row_of, b.src_tok, b.xp, b.xp_sf, b.perm_ws, b.perm_ws_bytes, s, to_f16);
-  MOE_TRY(moe_route_ex(logits, T, E, k, renorm, b.idx, b.w, s));
-  return permute_launch(b.idx, T, k, E, x_rows, row_bytes, x_sf, sf_bytes, b.counts, b.offsets, b.row_of, b.src_tok,
-                        b.xp, b.xp_sf, b.perm_ws, b.perm_ws_bytes, s, to_f16);
+  return route_permute_launch(logits, T, E, k, renorm, b.idx, b.w, x_rows, row_bytes, x_sf, sf_bytes, b.counts,
+                              b.offsets, b.row_of, b.src_tok, b.xp, b.xp_sf, b.perm_ws, b.perm_ws_bytes, s, to_f16);
 }
 
 // bytes of n MX-coded elements (MXFP4 packs two per byte)
@@ -110,7 +98,7 @@ size_t carve(const moe_layer* L, int T, void* ws, size_t cap, FwdBufs* b) {
   b->offsets = c.take<int32_t>(L->E + 1);
   b->row_of = c.take<int32_t>(Tk);
   b->src_tok = c.take<int32_t>(Tk);
-  b->perm_ws_bytes = std::max(permute_ws_bytes(T, L->k, L->E), route_permute_ws_bytes(T, L->E));
+  b->perm_ws_bytes = route_permute_ws_bytes(T, L->E);
   b->perm_ws = c.take<uint8_t>(b->perm_ws_bytes);
   b->xq = b->xsf = nullptr;
   b->gx = nullptr;
