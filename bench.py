@@ -46,8 +46,10 @@ CFG = synth.QWEN3_235B
 T_MAIN = 8192
 T_DECODE = 256
 UNIT = "tokens/s"
-# nominal dense FP4 / bf16 tensor throughput ratio of GB300 (13.5 / 2.25 PFLOP/s)
+# nominal dense FP4 / bf16 and FP8 / bf16 tensor throughput ratios of GB300
+# (13.5 / 2.25 and 4.5 / 2.25 PFLOP/s)
 FP4_OVER_BF16 = 6.0
+FP8_OVER_BF16 = 2.0
 
 # Profiling case for ncu captures: same H, k, I and rows per expert as the
 # main workload (T*k/E = 512), 32 experts and T=2048 (1.2 GB of weights).
@@ -230,7 +232,9 @@ def workload(args):
 
 # ------------------------------------------------------------------ model
 def bytes_per_elem(fmt: str) -> float:
-    return 2.0 if fmt == "bf16" else 0.5625  # NVFP4: 4-bit code + one E4M3 byte per 16
+    # NVFP4: 4-bit code + one E4M3 byte per 16; MXFP8: one byte + one E8M0 byte
+    # per 32; MXFP4: 4-bit code + one E8M0 byte per 32
+    return {"bf16": 2.0, "nvfp4": 0.5625, "mxfp8": 1.03125, "mxfp4": 0.53125}[fmt]
 
 
 def gemm_work(cfg, T, active_experts):
@@ -254,6 +258,10 @@ def gemm_kernel_name(cfg):
     and I, to be a multiple of 256)."""
     if cfg.w_fmt == "bf16" and cfg.act_fmt == "bf16":
         return "grouped_gemm_pair_kernel"
+    if cfg.w_fmt == "mxfp8":
+        return "grouped_gemm_mxf8_kernel"
+    if cfg.w_fmt == "mxfp4":
+        return "grouped_gemm_mxf4_kernel"
     k256 = cfg.H % 256 == 0 and cfg.I % 256 == 0 and cfg.I_s % 256 == 0
     if cfg.w_fmt == "nvfp4" and cfg.act_fmt == "nvfp4":
         return "grouped_gemm_nvf4w_kernel" if k256 else "grouped_gemm_nvf4_kernel"
@@ -264,8 +272,10 @@ def tensor_peak(cfg, p):
     """Dense tensor peak of the MMA the path runs: bf16 (bf16 layers and the
     NVFP4-weight / bf16-activation layer, whose MMA is bf16), or NVFP4 (both
     operands NVFP4: block-scaled FP4 MMA) = measured bf16 x the nominal ratio."""
-    if cfg.w_fmt == "nvfp4" and cfg.act_fmt == "nvfp4":
-        return p["bf16_tflops"] * FP4_OVER_BF16, "nvfp4", f"bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16)"
+    if (cfg.w_fmt, cfg.act_fmt) in (("nvfp4", "nvfp4"), ("mxfp4", "mxfp4")):
+        return p["bf16_tflops"] * FP4_OVER_BF16, cfg.w_fmt, f"bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16)"
+    if cfg.w_fmt == "mxfp8":
+        return p["bf16_tflops"] * FP8_OVER_BF16, "mxfp8", f"bf16_tflops x {FP8_OVER_BF16:g} (nominal fp8/bf16)"
     return p["bf16_tflops"], "bf16", "bf16_tflops (burst)"
 
 
@@ -373,11 +383,12 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
-# The NVFP4 workloads measured on the default run besides the benchmark
-# line's own (each carries its own roofline): the Qwen3.5-397B-shaped layer
-# (NVFP4 weights, bf16 activations) at decode and prefill sizes and the
-# DeepSeek-V3-shaped layer (NVFP4 weights and activations).
-EXTRA_POINTS = (("qwen35-397b", (64, 512, 4096)), ("deepseek-v3", (256, 16384)))
+# The NVFP4 and MX workloads measured on the default run besides the
+# benchmark line's own (each carries its own roofline): the Qwen3.5-397B-
+# shaped layer (NVFP4 weights, bf16 activations) at decode and prefill sizes,
+# the DeepSeek-V3-shaped layer (NVFP4 weights and activations), and the
+# Qwen3-235B-shaped layer in MXFP8 (the format the pages serve it in).
+EXTRA_POINTS = (("qwen35-397b", (64, 512, 4096)), ("deepseek-v3", (256, 16384)), ("qwen3-235b-mxfp8", (256, 8192)))
 EXTRA_STEPS = 20
 STAGES = ["quant", "dispatch", "gemm_gate_up", "gemm_down", "combine"]
 N_EVENTS = len(STAGES) + 1

@@ -13,6 +13,8 @@ shapes are those of the workloads the pages talk about:
   deepseek-v3 H=7168, E=256, top-8,  I=2048, one shared expert (I_s=2048),
               NVFP4 weights and NVFP4 activations
               ("Driving vLLM WideEP ... on Blackwell (Part I)")
+  qwen3-235b-mxfp8  the qwen3-235b shapes with MXFP8 weights and activations
+              ("Hosting Qwen on Blackwell", section "Quantização")
 
 Recipe (seed s):
   x       ~ N(0, 1) fp32 drawn with torch.Generator('cpu').manual_seed(s); on
@@ -23,8 +25,9 @@ Recipe (seed s):
             seeded permutation of 1..E and z the Zipf exponent (z=0: uniform).
   weights ~ N(0, 0.02) fp32 rounded to bf16, drawn per expert with
             torch.Generator(device).manual_seed(s + 1000) (device 'cuda' on the
-            GPU, 'cpu' for CPU-only tests).  NVFP4 weights are the bf16 master
-            passed through an NVFP4 quantiser by whoever consumes them.
+            GPU, 'cpu' for CPU-only tests).  NVFP4 / MX weights are the bf16
+            master passed through the format's quantiser by whoever consumes
+            them.
 """
 from __future__ import annotations
 
@@ -44,8 +47,8 @@ class LayerConfig:
     k: int
     I: int
     I_s: int            # 0: no shared expert
-    w_fmt: str          # 'bf16' | 'nvfp4'
-    act_fmt: str        # 'bf16' | 'nvfp4'
+    w_fmt: str          # 'bf16' | 'nvfp4' | 'mxfp8' | 'mxfp4'
+    act_fmt: str        # 'bf16' | 'nvfp4' | 'mxfp8' | 'mxfp4'
     zipf: float = 1.1
     outlier_p: float = 0.0
     Ts: Tuple[int, ...] = ()
@@ -68,7 +71,13 @@ QWEN35_397B = LayerConfig("qwen35-397b", 4096, 512, 10, 1024, 1024, "nvfp4", "bf
 DEEPSEEK_V3 = LayerConfig("deepseek-v3", 7168, 256, 8, 2048, 2048, "nvfp4", "nvfp4", 1.1, 0.001,
                           (256, 16384), h_amax=128.0)
 
-CONFIGS = {c.name: c for c in (TINY, QWEN3_235B, QWEN35_397B, DEEPSEEK_V3)}
+# the Qwen3-235B-shaped layer in MXFP8 weights and activations (E4M3 elements,
+# one E8M0 scale per 32), the format "Hosting Qwen on Blackwell" (section
+# "Quantização") serves that model in
+QWEN3_235B_MXFP8 = LayerConfig("qwen3-235b-mxfp8", 4096, 128, 8, 1536, 0, "mxfp8", "mxfp8", 1.1, 0.0,
+                               (256, 8192))
+
+CONFIGS = {c.name: c for c in (TINY, QWEN3_235B, QWEN35_397B, DEEPSEEK_V3, QWEN3_235B_MXFP8)}
 
 # size / imbalance sweep on the DeepSeek-V3 shapes
 SWEEP_TS = tuple(2 ** i for i in range(17))
