@@ -259,7 +259,7 @@ def gemm_kernel_name(cfg):
     if cfg.w_fmt == "bf16" and cfg.act_fmt == "bf16":
         return "grouped_gemm_pair_kernel"
     if cfg.w_fmt == "mxfp8":
-        return "grouped_gemm_mxf8_kernel"
+        return "grouped_gemm_mxf8p_kernel"
     if cfg.w_fmt == "mxfp4":
         return "grouped_gemm_mxf4_kernel"
     k256 = cfg.H % 256 == 0 and cfg.I % 256 == 0 and cfg.I_s % 256 == 0

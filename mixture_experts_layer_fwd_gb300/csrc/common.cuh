@@ -191,7 +191,17 @@ DEVINL void cp_async_4(uint32_t dst_smem, const void* src, bool valid) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst_smem), "l"(src), "r"(valid ? 4 : 0)
                : "memory");
 }
+// The same for 8 bytes (8-byte aligned addresses).
+DEVINL void cp_async_8(uint32_t dst_smem, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst_smem), "l"(src), "r"(valid ? 8 : 0)
+               : "memory");
+}
 DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+DEVINL uint2 ld_shared_u2(uint32_t saddr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr) : "memory");
+  return v;
+}
 template <int N>
 DEVINL void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");

@@ -461,7 +461,7 @@ int grouped_gemm_launch(int epi, int a_fmt, int w_fmt, const GemmProblem& routed
     MOE_TRY(check_problem_mx(routed, mx8, epi == MOE_EPI_SWIGLU_MX));
     if (sh) MOE_TRY(check_problem_mx(*sh, mx8, epi == MOE_EPI_SWIGLU_MX));
     if (routed.a_rows == 0) return MOE_OK;
-    if (mx8) return grouped_gemm_launch_mxf8(epi, routed, offsets, G, sh, shared_rows, s);
+    if (mx8) return grouped_gemm_launch_mxf8_pair(epi, routed, offsets, G, sh, shared_rows, s);
     return grouped_gemm_launch_mxf4(epi, routed, offsets, G, sh, shared_rows, s);
   }
   if (epi == MOE_EPI_SWIGLU_MX) return MOE_ERR_UNSUPPORTED;  // MX operands only

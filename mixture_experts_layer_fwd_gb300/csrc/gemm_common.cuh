@@ -86,9 +86,9 @@ struct PairTile {
 // (weights on the MMA's M side, tokens on N), token blocks fastest so that
 // the pairs working at the same time share a weight block through L2.  A
 // group of `rows` rows has ceil(rows/TM) token blocks of ng rows each (ng =
-// rows / blocks rounded up to 16, the MMA's N granularity); the last one
-// takes the remainder.
-// NQ: the MMA's N is the block's rows rounded up to a multiple of NQ.
+// rows / blocks rounded up to NQ, the MMA's N granularity: 16, or 32 for the
+// block-scaled MMAs); the last one takes the remainder, its N rounded up to
+// NQ.  TM is a multiple of NQ.
 template <int TM, int NQ = 16>
 DEVINL PairTile decode_pair_tile(int t, const int* s_prefix, const int* s_off, int GT, int G, int shared_rows) {
   int lo = 0, hi = GT;
@@ -103,7 +103,8 @@ DEVINL PairTile decode_pair_tile(int t, const int* s_prefix, const int* s_off, i
   const int start = routed ? s_off[lo] : 0;
   const int rows = routed ? (s_off[lo + 1] - s_off[lo]) : shared_rows;
   const int nb = (rows + TM - 1) / TM;
-  const int ng = ((rows + nb - 1) / nb + 15) & ~15;
+  static_assert(TM % NQ == 0 && (NQ & (NQ - 1)) == 0, "token blocks are whole MMA N steps");
+  const int ng = ((rows + nb - 1) / nb + NQ - 1) & ~(NQ - 1);
   const int local = t - s_prefix[lo];
   ti.blk = local / nb;
   const int m = local - ti.blk * nb;

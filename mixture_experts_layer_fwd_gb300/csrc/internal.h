@@ -74,8 +74,9 @@ int grouped_gemm_launch_nvf4_wide(int epi, const GemmProblem& routed, const int3
 int grouped_gemm_launch_mxf4(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                              const GemmProblem* sh, int shared_rows, cudaStream_t s);
 // Both operands MXFP8 (E4M3 bytes, E8M0 scales per 32), K % 256 == 0, bf16
-// epilogues (gemm_mxf8.cu).
-int grouped_gemm_launch_mxf8(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
-                             const GemmProblem* sh, int shared_rows, cudaStream_t s);
+// and MX SwiGLU epilogues, on CTA pairs: weights on the MMA's M side and
+// tokens on N (gemm_mxf8p.cu).
+int grouped_gemm_launch_mxf8_pair(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
+                                  const GemmProblem* sh, int shared_rows, cudaStream_t s);
 
 }  // namespace moe

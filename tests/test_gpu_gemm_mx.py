@@ -44,6 +44,8 @@ def _ref(A, W, offs, swiglu, N):
     ("mxfp8", 0, 448, 768, [0, 1, 127, 129, 300, 0, 40]),
     ("mxfp8", 1, 256, 1280, [300, 0, 513, 257, 64, 130]),
     ("mxfp8", 1, 192, 256, [7, 0, 260]),
+    ("mxfp8", 0, 256, 512, [192, 193, 385, 31, 33, 1000]),  # token blocks of the pair kernel
+    ("mxfp8", 1, 384, 512, [192, 193, 385, 31, 33, 1000]),
 ])
 def test_grouped_gemm_mx(fmt, epi, N, K, counts):
     import mixture_experts_layer_fwd_gb300 as m
@@ -71,6 +73,7 @@ def test_grouped_gemm_mx(fmt, epi, N, K, counts):
     ("mxfp4", 256, 1536, [300, 0, 513, 257, 64, 130]),
     ("mxfp8", 128, 256, [128]),
     ("mxfp8", 192, 1280, [7, 0, 260, 129]),
+    ("mxfp8", 256, 512, [192, 193, 385, 31, 33, 1000]),
 ])
 def test_grouped_gemm_mx_swiglu_mx_epilogue(fmt, N, K, counts):
     """SWIGLU_MX: the epilogue quantises the fp32 SwiGLU output to the MX
