@@ -46,9 +46,13 @@
 //                 previous MMAs are done (its empty barrier), write the slot,
 //                 arrive on the leader's full barrier
 //   warp 1        tensor-memory allocation of the pair; in the leader only,
-//                 the MMA issuer: 8 x tcgen05.mma.cta_group::2 (M=256, N=tile
-//                 tokens, K=32) per stage, commits multicast to both CTAs'
-//                 empty / tfull barriers
+//                 the MMA issuer, a whole converged warp: 8 x
+//                 tcgen05.mma.cta_group::2 (M=256, N=tile tokens, K=32) per
+//                 stage, commits multicast to both CTAs' empty / tfull
+//                 barriers; it starts each stage on a named-barrier signal
+//   warp 11       in the leader only: the MMA warp's waits (full barrier of
+//                 each stage, accumulator drained at a tile's start), so
+//                 that no mbarrier wait queues behind the issued MMAs
 //   warps 2..5    epilogue: each CTA reads its 128 accumulator lanes (weight
 //                 rows) x tokens and stores bf16 C[token, col] (STORE,
 //                 SWIGLU_BF16) or MXFP8 h (SWIGLU_MX: 32 x 32 chunks
@@ -87,30 +91,34 @@ constexpr int STAGE_BYTES = OFF_B + KSUB * B_TILE;  // 56 KB
 constexpr int STAGES = 3;
 constexpr uint32_t TX_CODES_PAIR = 2u * STAGE_BYTES;  // both CTAs' copies, counted on the leader
 constexpr int ACC_STRIDE = 256;            // accumulator buffers at columns 0 and 256
-constexpr int SF_SLOT_COLS = 32;
-constexpr int SFB_OFF = 8;                 // B scales after A's 2 cells x 4 columns
-constexpr int NUM_WARPS = 11;
+constexpr int SF_WORDS = KSUB;             // 32-bit scale words per row and stage (4 MMAs each)
+constexpr int SFB_OFF = 4 * SF_WORDS;      // B scales after A's cells x 4 columns
+constexpr int SF_SLOT_COLS = KSUB == 1 ? 16 : 32;
+constexpr int SF_GAP0 = (ACC_STRIDE - TN) / SF_SLOT_COLS;  // slots after the first accumulator
+constexpr int NUM_WARPS = 12;
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int TMEM_COLS = 512;
-constexpr int W_PROD_B = 6, W_SCALE0 = 7;
+constexpr int W_PROD_B = 6, W_SCALE0 = 7, W_WAIT = 11;
+constexpr int MMA_BAR = 4;                 // named barrier of the MMA warp and the wait warp
 constexpr int EXTRA = (2048 + 4 * (2 * MAX_G + 8) + 15) & ~15;
 constexpr int XCH_FLOATS = 32 * 32;                // one 32-lane x 32-token chunk
 constexpr int XCH_BYTES = 2 * 2 * XCH_FLOATS * 4;  // 2 warp pairs x 2 directions
-constexpr int SF_DEPTH = 3;                         // scale stages in the shared-memory ring
+constexpr int SF_DEPTH = STAGES;                    // scale stages in the shared-memory ring
 constexpr int SF_A_ROWS = WM;                       // ring slot: 128 weight rows, then TN token rows
-constexpr int SF_SLOT_BYTES = (SF_A_ROWS + TN) * 8; // 8 scale bytes per row and stage
+constexpr int SF_ROW_BYTES = 4 * SF_WORDS;          // scale bytes per row and stage
+constexpr int SF_SLOT_BYTES = (SF_A_ROWS + TN) * SF_ROW_BYTES;
 constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA + XCH_BYTES + 64 + SF_DEPTH * SF_SLOT_BYTES;
 static_assert(STAGE_BYTES % 1024 == 0 && B_TILE % 1024 == 0, "tiles must keep 1024-byte alignment");
-static_assert(MMAS == 8 && KSUB == 2, "a stage's scales are two 32-bit words per row");
-static_assert(SFB_OFF + 8 + 8 <= SF_SLOT_COLS && TN / 32 <= 8, "B scales fit the slot");
-static_assert(TN + 2 * SF_SLOT_COLS <= ACC_STRIDE && ACC_STRIDE + TN + SF_SLOT_COLS <= TMEM_COLS,
+static_assert(KSUB == 1 || KSUB == 2, "a stage's scales are one or two 32-bit words per row");
+static_assert(SFB_OFF + 8 * (SF_WORDS - 1) + TN / 32 <= SF_SLOT_COLS, "B scales fit the slot");
+static_assert(ACC_STRIDE + TN + (STAGES - SF_GAP0) * SF_SLOT_COLS <= TMEM_COLS,
               "scale slots fit the gaps after the accumulators");
 static_assert(TN > 128 && TN <= 256, "the 128 scale threads copy one weight row and one or two token rows");
 static_assert(SMEM <= 232448, "shared memory budget");
 
 // tensor-memory column of stage s's scale slot
 DEVINL uint32_t sf_slot(int s) {
-  return s == 0 ? TN : (s == 1 ? TN + SF_SLOT_COLS : ACC_STRIDE + TN);
+  return s < SF_GAP0 ? TN + s * SF_SLOT_COLS : ACC_STRIDE + TN + (s - SF_GAP0) * SF_SLOT_COLS;
 }
 
 // Instruction descriptor, kind::mxf8f6f4 with E8M0 scales: E4M3 x E4M3 ->
@@ -121,15 +129,38 @@ DEVINL uint32_t idesc_mxf8(int M, int N, uint32_t sf_id) {
          (static_cast<uint32_t>(M >> 4) << 24) | (sf_id << 29);
 }
 
-DEVINL void umma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
-                           uint32_t sfb_tmem, uint32_t accumulate) {
+// Issued by a whole converged warp: every lane computes the (warp-uniform)
+// operands and elect.sync picks the one lane that issues, which costs far
+// less per MMA than a single-lane branch; these MMAs are short (about 55 ns
+// of tensor work at N = 192), so a single lane's issue would set the pace.
+DEVINL void umma_mxf8_pair_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                                uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+      "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
+}
+
+// Bounded wait of a whole warp on a barrier whose completions publish
+// tensor-memory state from both CTAs (relaxed cluster-scope test).
+DEVINL bool wait_cluster_warp(uint64_t* bar, uint32_t parity, unsigned long long tmo, unsigned int* err,
+                              volatile int* abort) {
+  bool done = mbar_try_wait_relaxed_cluster(bar, parity);
+  const uint64_t t0 = globaltimer_ns();
+  while (!__all_sync(0xFFFFFFFFu, done)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > tmo) {
+      if ((threadIdx.x & 31) == 0) atomicOr(err, kErrTimeout);
+      *abort = 1;
+      return false;
+    }
+    done = done || mbar_try_wait_relaxed_cluster(bar, parity);
+  }
+  return true;
 }
 
 template <int EPI>
@@ -232,9 +263,12 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8p_kernel(const __
     }
   } else if (warp == 1) {
     // ===================================================== MMA issuer (leader)
-    if (lane == 0 && leader) {
+    // The whole warp walks the schedule and issues; each stage starts on the
+    // go signal of the wait warp (both CTAs' codes and scales in place and,
+    // on a tile's first stage, the accumulator drained), so this warp never
+    // waits on an mbarrier between its MMAs.
+    if (leader) {
       int stage = 0;
-      uint32_t phase = 0;
       bool ok = true;
       int it = 0;
       const uint64_t a_desc0 = smem_desc_kmajor_sw128(smem_u32(stages));
@@ -246,25 +280,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8p_kernel(const __
 #pragma unroll
         for (int i = 0; i < 4; ++i) idesc[i] = idesc_mxf8(2 * WM, ti.n, static_cast<uint32_t>(i));
         const int buf = it & 1;
-        const uint32_t use = static_cast<uint32_t>(it >> 1);
-        // both CTAs' epilogues must have drained this accumulator buffer
-        {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait_relaxed_cluster(&tempty[buf], (use & 1u) ^ 1u)) {
-            if (*abort_flag || globaltimer_ns() - t0 > tmo) {
-              atomicOr(p.err, kErrTimeout);
-              *abort_flag = 1;
-              ok = false;
-              break;
-            }
-          }
-          if (!ok) break;
-        }
-        tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * ACC_STRIDE);
         for (int kb = 0; kb < nk; ++kb) {
-          // codes of both CTAs landed and all 8 scale warps wrote the slot
-          if (!mbar_wait_bounded(&full[stage], phase, tmo, p.err, abort_flag)) {
+          if (named_bar_red_or(MMA_BAR, 64, false)) {
             ok = false;
             break;
           }
@@ -275,25 +293,51 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8p_kernel(const __
 #pragma unroll
           for (int m = 0; m < MMAS; ++m) {
             const int j = m >> 2, kk = m & 3;  // k-block, 32-byte step inside it
-            umma_mxf8_pair(d, da + ((j * A_TILE + kk * 32) >> 4), db + ((j * B_TILE + kk * 32) >> 4), idesc[kk],
-                           sf_t + 4 * j, sf_t + SFB_OFF + 8 * j, (kb | m) ? 1u : 0u);
+            umma_mxf8_pair_warp(d, da + ((j * A_TILE + kk * 32) >> 4), db + ((j * B_TILE + kk * 32) >> 4),
+                                idesc[kk], sf_t + 4 * j, sf_t + SFB_OFF + 8 * j, (kb | m) ? 1u : 0u);
           }
-          umma_commit_pair_multicast(&empty[stage], 0x3);
+          umma_commit_pair_multicast_warp(&empty[stage], 0x3);
+          if (++stage == S) stage = 0;
+        }
+        if (ok) umma_commit_pair_multicast_warp(&tfull[buf], 0x3);
+      }
+      if (!ok && lane == 0) {
+        umma_commit_pair_multicast(drain, 0x1);
+        mbar_wait_bounded(drain, 0, 1000000000ull, p.err, nullptr);
+      }
+    }
+  } else if (warp == W_WAIT) {
+    // ===================================================== waits for the MMA warp (leader)
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < total && ok; t += n_clusters, ++it) {
+        const gg::PairTile ti = gg::decode_pair_tile<TN, NQ>(t, s_prefix, s_off, GT, G, p.shared_rows);
+        const int nk = p.prob[ti.pb].K / KE;
+        const int buf = it & 1;
+        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        for (int kb = 0; kb < nk; ++kb) {
+          // kb == 0: both CTAs' epilogues have drained this accumulator
+          // buffer; every stage: codes of both CTAs landed and all 8 scale
+          // warps wrote the slot
+          const bool good = (kb > 0 || wait_cluster_warp(&tempty[buf], (use & 1u) ^ 1u, tmo, p.err, abort_flag)) &&
+                            mbar_wait_warp(&full[stage], phase, tmo, p.err, abort_flag);
+          if (named_bar_red_or(MMA_BAR, 64, !good)) {
+            ok = false;
+            break;
+          }
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit_pair_multicast(&tfull[buf], 0x3);
-      }
-      if (!ok) {
-        umma_commit_pair_multicast(drain, 0x1);
-        mbar_wait_bounded(drain, 0, 1000000000ull, p.err, nullptr);
       }
     }
   } else if (warp >= W_SCALE0) {
     // ===================================================== scale warps (7..10)
-    // The 128 threads copy each stage's 8 scale bytes of the CTA's 128
+    // The 128 threads copy each stage's scale bytes of the CTA's 128
     // weight rows and the tile's 192 token rows (one to three rows each)
     // into a ring of SF_DEPTH slots in shared memory with cp.async, SF_DEPTH
     // - 1 stages ahead of the stage they write to tensor memory; after a
@@ -338,14 +382,20 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8p_kernel(const __
     };
     // copies the cursor's stage into ring slot `slot` and advances; commits
     // a (possibly empty) group either way so that group counts stay uniform
+    auto copy_row = [&](uint32_t dst, const uint8_t* row, int off) {
+      if (SF_ROW_BYTES == 8)
+        cp_async_8(dst, row ? row + off : any, row != nullptr);
+      else
+        cp_async_4(dst, row ? row + off : any, row != nullptr);
+    };
     auto issue = [&](int slot) -> bool {
       const bool has = ct < total;
       if (has) {
-        const uint32_t d = ring + static_cast<uint32_t>(slot * SF_SLOT_BYTES + st * 8);
-        const int off = ckb * 8;
-        cp_async_8(d, rp[0] ? rp[0] + off : any, rp[0] != nullptr);
-        cp_async_8(d + SF_A_ROWS * 8, rp[1] ? rp[1] + off : any, rp[1] != nullptr);
-        if (st + 128 < TN) cp_async_8(d + (SF_A_ROWS + 128) * 8, rp[2] ? rp[2] + off : any, rp[2] != nullptr);
+        const uint32_t d = ring + static_cast<uint32_t>(slot * SF_SLOT_BYTES + st * SF_ROW_BYTES);
+        const int off = ckb * SF_ROW_BYTES;
+        copy_row(d, rp[0], off);
+        copy_row(d + SF_A_ROWS * SF_ROW_BYTES, rp[1], off);
+        if (st + 128 < TN) copy_row(d + (SF_A_ROWS + 128) * SF_ROW_BYTES, rp[2], off);
         if (++ckb == cnk) {
           ct += n_clusters;
           open_tile();
@@ -369,25 +419,28 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8p_kernel(const __
       // slot refilled next
       named_bar_sync(3, 128);
       pending += issue(slot == 0 ? SF_DEPTH - 1 : slot - 1) ? 1 : 0;
-      uint32_t r[32];
+      // column 4w + c: word w of weight row lane + 32c; column SFB_OFF + 8w
+      // + c: word w of token row lane + 32c
+      uint32_t r[SF_SLOT_COLS];
+#pragma unroll
+      for (int i = 0; i < SF_SLOT_COLS; ++i) r[i] = 0u;
       {
-        const uint32_t d = ring + static_cast<uint32_t>(slot * SF_SLOT_BYTES + lane * 8);
+        const uint32_t d = ring + static_cast<uint32_t>(slot * SF_SLOT_BYTES + lane * SF_ROW_BYTES);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint2 a = ld_shared_u2(d + c * 256);
-          r[c] = a.x;
-          r[4 + c] = a.y;
+        for (int c = 0; c < 4 + TN / 32; ++c) {
+          const bool is_a = c < 4;
+          const uint32_t a = d + static_cast<uint32_t>((is_a ? 32 * c : SF_A_ROWS + 32 * (c - 4)) * SF_ROW_BYTES);
+          uint32_t w[SF_WORDS];
+          if constexpr (SF_WORDS == 2) {
+            const uint2 v = ld_shared_u2(a);
+            w[0] = v.x;
+            w[SF_WORDS - 1] = v.y;
+          } else {
+            w[0] = ld_shared_u32(a);
+          }
+#pragma unroll
+          for (int i = 0; i < SF_WORDS; ++i) r[is_a ? 4 * i + c : SFB_OFF + 8 * i + (c - 4)] = w[i];
         }
-#pragma unroll
-        for (int c = 0; c < TN / 32; ++c) {
-          const uint2 b = ld_shared_u2(d + (SF_A_ROWS + 32 * c) * 8);
-          r[SFB_OFF + c] = b.x;
-          r[SFB_OFF + 8 + c] = b.y;
-        }
-#pragma unroll
-        for (int c = TN / 32; c < 8; ++c) r[SFB_OFF + c] = r[SFB_OFF + 8 + c] = 0u;
-#pragma unroll
-        for (int c = SFB_OFF + 16; c < 32; ++c) r[c] = 0u;
       }
       --pending;
       if (++slot == SF_DEPTH) slot = 0;
@@ -396,7 +449,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8p_kernel(const __
       if (ok) ok = mbar_wait_warp(&empty[stage], phase ^ 1u, tmo, p.err, abort_flag);
       if (ok) {
         tc_fence_after();
-        tmem_st_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + sf_slot(stage), r);
+        tmem_st_32x32b(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + sf_slot(stage), r);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
