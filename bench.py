@@ -252,10 +252,12 @@ def gemm_work(cfg, T, active_experts):
     return flops, weights + acts, weights
 
 
-def gemm_kernel_name(cfg):
-    """The grouped-GEMM kernel a layer's formats and shapes dispatch to (the
+def gemm_kernel_name(cfg, T=None):
+    """The grouped-GEMM kernels a layer's formats and shapes dispatch to (the
     NVFP4 kernels with 256-element k stages need every reduction length, H
-    and I, to be a multiple of 256)."""
+    and I, to be a multiple of 256; with 512-element multiples and at least
+    64 routed rows per expert on average, the down projection takes the
+    CTA-pair kernel)."""
     if cfg.w_fmt == "bf16" and cfg.act_fmt == "bf16":
         return "grouped_gemm_pair_kernel"
     if cfg.w_fmt == "mxfp8":
@@ -264,6 +266,9 @@ def gemm_kernel_name(cfg):
         return "grouped_gemm_mxf4_kernel"
     k256 = cfg.H % 256 == 0 and cfg.I % 256 == 0 and cfg.I_s % 256 == 0
     if cfg.w_fmt == "nvfp4" and cfg.act_fmt == "nvfp4":
+        k512 = cfg.H % 512 == 0 and cfg.I % 512 == 0 and cfg.I_s % 512 == 0
+        if k512 and T is not None and T * cfg.k >= 64 * cfg.E:
+            return "grouped_gemm_nvf4w_kernel (gate/up) + grouped_gemm_nvf4p_kernel (down)"
         return "grouped_gemm_nvf4w_kernel" if k256 else "grouped_gemm_nvf4_kernel"
     return "grouped_gemm_w4a16_kernel" if k256 else "grouped_gemm_kernel"
 
@@ -298,7 +303,7 @@ def roofline(cfg, T, gemm_ms, active, traffic, src):
              "frac": round(ach / p["hbm_gbs"], 4), "peak_source": f"hbm_gbs of {src} peaks",
              "algorithmic": f"{nbytes / 2 / 1e9:.3f} GB per launch ({wbytes / 1e9:.3f} GB of weights of "
                             f"{active} active experts per step)"}
-    r.update({"traffic": traffic, "kernel": f"{gemm_kernel_name(cfg)} (2 launches/step)", "mma": mma,
+    r.update({"traffic": traffic, "kernel": f"{gemm_kernel_name(cfg, T)} (2 launches/step)", "mma": mma,
               "t_roof_ms": round(max(t_tensor, t_hbm) * 1e3, 4)})
     return r
 

@@ -349,6 +349,24 @@ DEVINL bool mbar_try_wait_relaxed_cluster(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+
+// Bounded wait of a whole warp on a barrier whose completions publish
+// tensor-memory state from both CTAs (relaxed cluster-scope test).
+DEVINL bool wait_cluster_warp(uint64_t* bar, uint32_t parity, unsigned long long tmo, unsigned int* err,
+                              volatile int* abort) {
+  bool done = mbar_try_wait_relaxed_cluster(bar, parity);
+  const uint64_t t0 = globaltimer_ns();
+  while (!__all_sync(0xFFFFFFFFu, done)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > tmo) {
+      if ((threadIdx.x & 31) == 0) atomicOr(err, kErrTimeout);
+      *abort = 1;
+      return false;
+    }
+    done = done || mbar_try_wait_relaxed_cluster(bar, parity);
+  }
+  return true;
+}
 DEVINL void tma_load_3d_pair(const void* tmap, uint32_t bar_cluster_addr, void* smem_dst, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "

@@ -145,24 +145,6 @@ DEVINL void umma_mxf8_pair_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
       : "memory");
 }
 
-// Bounded wait of a whole warp on a barrier whose completions publish
-// tensor-memory state from both CTAs (relaxed cluster-scope test).
-DEVINL bool wait_cluster_warp(uint64_t* bar, uint32_t parity, unsigned long long tmo, unsigned int* err,
-                              volatile int* abort) {
-  bool done = mbar_try_wait_relaxed_cluster(bar, parity);
-  const uint64_t t0 = globaltimer_ns();
-  while (!__all_sync(0xFFFFFFFFu, done)) {
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > tmo) {
-      if ((threadIdx.x & 31) == 0) atomicOr(err, kErrTimeout);
-      *abort = 1;
-      return false;
-    }
-    done = done || mbar_try_wait_relaxed_cluster(bar, parity);
-  }
-  return true;
-}
-
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_mxf8p_kernel(const __grid_constant__ Params p) {
   constexpr int S = STAGES;

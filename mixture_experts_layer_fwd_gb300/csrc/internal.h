@@ -69,6 +69,11 @@ int grouped_gemm_launch_w4a16(int epi, const GemmProblem& routed, const int32_t*
                               const GemmProblem* sh, int shared_rows, cudaStream_t s);
 int grouped_gemm_launch_nvf4_wide(int epi, const GemmProblem& routed, const int32_t* offsets, int G,
                                   const GemmProblem* sh, int shared_rows, cudaStream_t s);
+// NVFP4 x NVFP4 down projection (bf16 output) on CTA pairs (weights on the
+// MMA's M side, tokens on N), K % 512 == 0 and 16-byte aligned scale arrays
+// (gemm_nvf4p.cu).
+int grouped_gemm_launch_nvf4_pair(const GemmProblem& routed, const int32_t* offsets, int G, const GemmProblem* sh,
+                                  int shared_rows, cudaStream_t s);
 // Both operands MXFP4 (E2M1 codes, E8M0 scales per 32), K % 512 == 0, bf16
 // epilogues (gemm_mxf4.cu).
 int grouped_gemm_launch_mxf4(int epi, const GemmProblem& routed, const int32_t* offsets, int G,

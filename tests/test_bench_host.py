@@ -43,6 +43,17 @@ def test_kernel_name_follows_the_dispatch(name, kernel):
     assert bench.gemm_kernel_name(synth.CONFIGS[name]) == kernel
 
 
+def test_kernel_name_nvfp4_prefill_down_projection_on_pairs():
+    """With >= 64 routed rows per expert and 512-multiples of H and I, the
+    NVFP4 down projection takes the CTA-pair kernel (decode keeps the 1-SM
+    kernel for both projections)."""
+    cfg = synth.CONFIGS["deepseek-v3"]
+    assert bench.gemm_kernel_name(cfg, 256) == "grouped_gemm_nvf4w_kernel"
+    assert bench.gemm_kernel_name(cfg, 16384) == ("grouped_gemm_nvf4w_kernel (gate/up) + "
+                                                  "grouped_gemm_nvf4p_kernel (down)")
+    assert bench.gemm_kernel_name(synth.CONFIGS["qwen3-235b-mxfp8"], 8192) == "grouped_gemm_mxf8p_kernel"
+
+
 def test_kernel_name_for_k_not_multiple_of_256():
     w4 = synth.small_variant(synth.QWEN35_397B, H=320, E=8, k=2, I=192, name="w4-odd")
     a4 = synth.small_variant(synth.DEEPSEEK_V3, H=320, E=8, k=2, I=192, name="a4-odd")
