@@ -33,6 +33,9 @@ struct Params {
   CUtensorMap tma_w[2];
   CUtensorMap tma_asf[2];  // scale rows of A / W (512-element-stage FP4 kernel)
   CUtensorMap tma_wsf[2];
+  // token boxes of 16, 32, ..., 128 rows (bf16 CTA-pair kernel: each CTA
+  // stages the half of a tile's tokens it needs, rounded up to 16 rows)
+  CUtensorMap tma_b_rows[2][8];
   Prob prob[2];
   const int32_t* offsets;  // [G+1] rows of each routed group in A
   int G;

@@ -21,9 +21,9 @@
 //
 // Roles (both CTAs of the pair run the same tile sequence):
 //   warp 0      TMA producer of this CTA: one box of its 128 weight rows x
-//               2 k-blocks and one box of 128 token rows (from its half of
-//               the tile's tokens on) x 2 k-blocks; rows past the half are
-//               staged and not read by the MMA; both copies complete on the
+//               2 k-blocks and one box of h token rows (from its half of
+//               the tile's tokens on; h = N/2 rounded up to 16, one tensor
+//               map per height) x 2 k-blocks; both copies complete on the
 //               leader CTA's full barrier, which the leader arms for both
 //   warp 1      TMEM allocation of the pair; in the leader only, the MMA
 //               issuer: 8 x tcgen05.mma.cta_group::2 (M=256, N=tile tokens,
@@ -56,12 +56,13 @@ constexpr int WM = 128;               // weight rows per CTA (M of the MMA is 2 
 constexpr int BK = 64;                // bf16 elements per k-block (128-byte rows)
 constexpr int GU_ROWS = 64;           // SwiGLU: features per CTA (64 gate + 64 up rows)
 constexpr int A_TILE = WM * BK * 2;   // 16 KB: this CTA's weight rows
-constexpr int B_ROWS = 128;           // token rows staged per CTA (>= half of N)
+constexpr int B_ROWS = 128;           // most token rows staged per CTA (half of the largest N)
+constexpr int B_STEP = 16;            // a tile stages ceil(N/2 / 16) * 16 token rows per CTA
 constexpr int B_TILE = B_ROWS * BK * 2;
 constexpr int KSUB = 2;               // k-blocks per pipeline stage (128 of K)
 constexpr int STAGES = 3;
 constexpr int STAGE_BYTES = KSUB * (A_TILE + B_TILE);  // [A k-block 0][A 1][B 0][B 1]
-constexpr uint32_t TX_BYTES_PAIR = 2 * STAGE_BYTES;    // both CTAs' loads, counted on the leader
+static_assert(B_ROWS / B_STEP == 8, "one token tensor map per box height");
 constexpr int NUM_WARPS = 6;
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int TMEM_COLS = 512;
@@ -131,20 +132,20 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
   if (warp == 0) {
     // ===================================================== TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&p.tma_a[0]);
       tma_prefetch_desc(&p.tma_w[0]);
-      if (p.shared_rows >= 0) {
-        tma_prefetch_desc(&p.tma_a[1]);
-        tma_prefetch_desc(&p.tma_w[1]);
-      }
+      if (p.shared_rows >= 0) tma_prefetch_desc(&p.tma_w[1]);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int t = cluster_id; t < total && ok; t += n_clusters) {
         const gg::PairTile ti = gg::decode_pair_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
         const Prob& P = p.prob[ti.pb];
-        const void* ta = &p.tma_a[ti.pb];
+        // this CTA's token box: the half of the tile's N it stages, rounded
+        // up to 16 rows (fewer staged bytes for small token blocks)
+        const int h = (((ti.n >> 1) + B_STEP - 1) / B_STEP) * B_STEP;
+        const void* ta = &p.tma_b_rows[ti.pb][h / B_STEP - 1];
         const void* tw = &p.tma_w[ti.pb];
+        const uint32_t tx = 2u * static_cast<uint32_t>(KSUB * (A_TILE + h * BK * 2));  // both CTAs, on the leader
         // this CTA's tokens start half of N into the tile (half <= 128)
         const int b_y = ti.row0 + static_cast<int>(rank) * (ti.n >> 1);
         // this CTA's 128 weight rows: SwiGLU -> gate and up rows of features
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
           const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
           // one copy per operand moves both k-blocks of the stage (a k-block
           // past the end of K is zero-filled and still counted)
-          if (leader) mbar_arrive_expect_tx(&full[stage], TX_BYTES_PAIR);
+          if (leader) mbar_arrive_expect_tx(&full[stage], tx);
           if (SWIGLU)
             tma_load_4d_pair(tw, fbar, sb, 0, f0, 2 * ti.g, kb);
           else
@@ -190,6 +191,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
         const gg::PairTile ti = gg::decode_pair_tile<TM>(t, s_prefix, s_off, GT, G, p.shared_rows);
         const int nk = p.prob[ti.pb].K / BK;
         const uint32_t idesc = idesc_bf16_f32(2 * WM, ti.n);
+        // second token k-block of a stage: after the first one's h rows
+        const uint64_t b_kblk = static_cast<uint64_t>(((((ti.n >> 1) + B_STEP - 1) / B_STEP) * B_STEP * BK * 2) >> 4);
         const int buf = it & 1;
         const uint32_t use = static_cast<uint32_t>(it >> 1);
         // both CTAs' epilogues must have drained this accumulator buffer
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_pair_kernel(const __g
           if (nsub > 1) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              umma_f16_pair(d, da + (A_TILE >> 4) + 2 * kk, db + (B_TILE >> 4) + 2 * kk, idesc, 1u);
+              umma_f16_pair(d, da + (A_TILE >> 4) + 2 * kk, db + b_kblk + 2 * kk, idesc, 1u);
           }
           umma_commit_pair_multicast(&empty[stage], 0x3);
           if (++stage == S) {
@@ -386,7 +389,9 @@ static int fill(Params& prm, int slot, int epi, const GemmProblem& P) {
   q.c_sf = nullptr;
   q.a_g = q.w_g = q.c_g = nullptr;
   q.a_sf = q.w_sf = nullptr;
-  MOE_TRY(encode_tmap_kblocks(&prm.tma_a[slot], P.A, P.K, static_cast<uint64_t>(P.a_rows), B_ROWS, KSUB));
+  for (int i = 0; i < B_ROWS / B_STEP; ++i)
+    MOE_TRY(encode_tmap_kblocks(&prm.tma_b_rows[slot][i], P.A, P.K, static_cast<uint64_t>(P.a_rows),
+                                static_cast<uint32_t>(B_STEP * (i + 1)), KSUB));
   if (epi == MOE_EPI_STORE_BF16)
     MOE_TRY(encode_tmap_kblocks(&prm.tma_w[slot], P.W, P.K, static_cast<uint64_t>(q.w_rows_total), WM, KSUB));
   else

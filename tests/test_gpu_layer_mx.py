@@ -18,12 +18,13 @@ DEV = "cuda"
 
 def mx_layer(fmt):
     """Small MX layers: Qwen3-235B-like (no shared expert) in MXFP8, the
-    format the pages serve it in, and DeepSeek-V3-like (shared expert) in
-    MXFP4."""
+    format the pages serve it in, and DeepSeek-V3-like (shared expert, the
+    shared problem of the same launch) in MXFP8 and MXFP4."""
     if fmt == "mxfp8":
         base = synth.small_variant(synth.QWEN3_235B, H=512, E=16, k=4, I=256, name="qwen3-mxfp8-small")
-    else:
-        base = synth.small_variant(synth.DEEPSEEK_V3, H=512, E=16, k=4, I=512, I_s=512, name="ds-mxfp4-small")
+        return dataclasses.replace(base, w_fmt=fmt, act_fmt=fmt)
+    base = synth.small_variant(synth.DEEPSEEK_V3, H=512, E=16, k=4, I=512, I_s=512, name=f"ds-{fmt}-small")
+    fmt = fmt.replace("-shared", "")
     return dataclasses.replace(base, w_fmt=fmt, act_fmt=fmt)
 
 
@@ -32,7 +33,7 @@ def _gpu():
     require_gpu()
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp8-shared", "mxfp4"])
 @pytest.mark.parametrize("T", [1, 37, 300])
 def test_mx_layer_all_tokens(fmt, T):
     from mixture_experts_layer_fwd_gb300 import MoELayer, moe_sync_status
