@@ -14,9 +14,8 @@
 // needs (128 + 128) bytes per element of K for 2 x 128 x 128 FLOPs, and the
 // shared-memory fill rate, not the tensor cores, sets its pace.  Here each
 // SM stages its 128 weight rows and 96 token rows: 224 bytes per element of
-// K for 2 x 128 x 192 FLOPs, the bytes per FLOP of the bf16 pair kernel.
-// Tokens on N also cut a group of r rows into ceil(r/192) equal blocks
-// rounded up to 16 instead of 128-row tiles.
+// K for 2 x 128 x 192 FLOPs.  Tokens on N also cut a group of r rows into
+// ceil(r/192) equal blocks rounded up to 32 instead of 128-row tiles.
 //
 // Stages: 256 elements of K (two 128-byte k-blocks per row): 32 KB of weight
 // codes and 24 KB of token codes per SM, by TMA (128-byte swizzle); 8 MMAs
@@ -31,10 +30,11 @@
 // 8..23 (column 8 + 8w + c, c < N/32).  Tensor memory holds two fp32
 // accumulators (columns 0..191 and 256..447) and, in the gaps, the three
 // stages' slots (columns 192, 224 and 448).  A stage's scales are 8 bytes per
-// row, under the 16-byte minimum of a TMA box, so the four scale warps of
-// each CTA read them straight from global memory (one 8-byte load per row,
-// issued before the wait for the slot; rows outside the operand or the tile
-// read as zero) and write the slot with one tcgen05.st.
+// row, under the 16-byte minimum of a TMA box: the 128 threads of the four
+// scale warps of each CTA copy each row once with cp.async into a ring in
+// shared memory, SF_DEPTH - 1 stages ahead (rows outside the operand or the
+// tile read as zero), and after a barrier of the four warps each warp writes
+// its lane quadrant of the slot with one tcgen05.st.
 //
 // Roles (both CTAs of the pair run the same tile sequence):
 //   warp 0        weight codes of this CTA's 128 rows (one 3-/4-D box: both
@@ -42,9 +42,10 @@
 //                 both CTAs' code bytes
 //   warp 6        token codes: 96 rows from this CTA's half of the tile on
 //                 (rows past the half are staged and not read by the MMA)
-//   warps 7..10   scale warps, one per lane quadrant: wait until the stage's
-//                 previous MMAs are done (its empty barrier), write the slot,
-//                 arrive on the leader's full barrier
+//   warps 7..10   scale warps, one per lane quadrant: ring of copies, wait
+//                 until the stage's previous MMAs are done (its empty
+//                 barrier), write the slot, arrive on the leader's full
+//                 barrier
 //   warp 1        tensor-memory allocation of the pair; in the leader only,
 //                 the MMA issuer, a whole converged warp: 8 x
 //                 tcgen05.mma.cta_group::2 (M=256, N=tile tokens, K=32) per
