@@ -13,13 +13,15 @@
 //   phase A  block b routes its contiguous token chunk (one warp per token),
 //            counts its slots per expert in shared memory -> hist[b][e]
 //   barrier
-//   phase B  one thread per expert scans the column hist[*][e]:
+//   phase B  one warp per expert scans the column hist[*][e] (32 blocks
+//            per step, all of a lane's loads in flight at once):
 //            base[b][e] = sum of hist[b'][e] over b' < b, counts[e] = total
 //   barrier
 //   phase C  every block scans counts (offsets; block 0 stores them), seeds
 //            its shared counters with offsets[e] + base[b][e], walks its
-//            slots in order (one warp, ranks from __match_any_sync) to write
-//            row_of / src_tok, then copies its slots' token rows
+//            slots in order (one warp, ranks from __match_any_sync, the next
+//            32 slots' expert ids loaded while the current ones are placed)
+//            to write row_of / src_tok, then copies its slots' token rows
 // A block's chunk is contiguous and blocks are ordered, so inside an expert
 // the rows stay in ascending token order.
 //
@@ -122,21 +124,32 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(const DispatchA
   for (int e = threadIdx.x; e < E; e += kThreads) a.hist[static_cast<size_t>(b) * E + e] = sh[e];
   if (!grid_barrier(a.bar, static_cast<unsigned int>(nb), a.timeout_ns, a.err, &s_ok)) return;
 
-  // ---- phase B: per-expert column scans over the blocks, the per-block
-  // counts read 8 at a time so that the loads overlap
-  for (int e = b * kThreads + threadIdx.x; e < E; e += nb * kThreads) {
-    int run = 0;
-    for (int c0 = 0; c0 < nb; c0 += 8) {
-      int h8[8];
+  // ---- phase B: per-expert column scans over the blocks, one warp per
+  // expert (expert b * kWarps + warp, so E / 32 blocks take part); lane l
+  // holds the counts of blocks l, l + 32, ... (nb <= kMaxBlocks)
+  for (int e = b * kWarps + warp; e < E; e += nb * kWarps) {
+    constexpr int kCols = kMaxBlocks / 32;
+    int h[kCols];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) h8[u] = c0 + u < nb ? __ldcg(a.hist + static_cast<size_t>(c0 + u) * E + e) : 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (c0 + u < nb) a.base[static_cast<size_t>(c0 + u) * E + e] = run;
-        run += h8[u];
-      }
+    for (int u = 0; u < kCols; ++u) {
+      const int c = u * 32 + lane;
+      h[u] = c < nb ? __ldcg(a.hist + static_cast<size_t>(c) * E + e) : 0;
     }
-    a.counts[e] = run;
+    int run = 0;
+#pragma unroll
+    for (int u = 0; u < kCols; ++u) {
+      if (u * 32 >= nb) break;
+      int incl = h[u];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const int c = u * 32 + lane;
+      if (c < nb) a.base[static_cast<size_t>(c) * E + e] = run + incl - h[u];
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) a.counts[e] = run;
   }
   if (!grid_barrier(a.bar, 2u * static_cast<unsigned int>(nb), a.timeout_ns, a.err, &s_ok)) return;
 
@@ -172,9 +185,11 @@ __global__ void __launch_bounds__(kThreads) route_permute_kernel(const DispatchA
   if (b == 0 && threadIdx.x == kThreads - 1) a.offsets[E] = run;  // the last thread's run is the total
   __syncthreads();
   if (warp == 0) {
+    int e_next = s0 + lane < s1 ? __ldcg(a.idx + s0 + lane) : 0;
     for (int j0 = s0; j0 < s1; j0 += 32) {
       const int s = j0 + lane;
-      const int e = s < s1 ? a.idx[s] : 0;
+      const int e = e_next;
+      e_next = j0 + 32 + lane < s1 ? __ldcg(a.idx + j0 + 32 + lane) : 0;
       const bool act = s < s1 && static_cast<unsigned>(e) < static_cast<unsigned>(E);
       const unsigned mask = __ballot_sync(0xFFFFFFFFu, act);
       if (act) {
