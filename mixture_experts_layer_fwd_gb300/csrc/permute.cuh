@@ -28,19 +28,35 @@ DEVINL void copy_row(const uint8_t* __restrict__ x, int row_bytes, const uint8_t
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * row_bytes);
   uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(r) * row_bytes);
   const int nvec = row_bytes >> 4;
-  int i = lane;
-  for (; i + 96 < nvec; i += 128) {
-    const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
-    dst[i] = cvt_row_vec(a, TO_F16);
-    dst[i + 32] = cvt_row_vec(b, TO_F16);
-    dst[i + 64] = cvt_row_vec(c, TO_F16);
-    dst[i + 96] = cvt_row_vec(d, TO_F16);
+  // the row's scale words (up to 128 of them: 512 scale bytes) are loaded
+  // first, so that their round trip overlaps the code vectors'
+  const int nsw = x_sf != nullptr ? (sf_bytes >> 2) : 0;
+  const uint32_t* ssrc = nsw ? reinterpret_cast<const uint32_t*>(x_sf + static_cast<size_t>(t) * sf_bytes) : nullptr;
+  uint32_t sv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (lane + 32 * u < nsw) sv[u] = __ldg(ssrc + lane + 32 * u);
+  // eight 16-byte loads of the lane in flight before its stores (one round
+  // trip per 256 vectors = 4 KB of the row)
+  for (int i0 = 0; i0 < nvec; i0 += 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      if (i < nvec) v[j] = __ldg(src + i);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      if (i < nvec) dst[i] = cvt_row_vec(v[j], TO_F16);
+    }
   }
-  for (; i < nvec; i += 32) dst[i] = cvt_row_vec(__ldg(src + i), TO_F16);
-  if (x_sf != nullptr) {
-    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(x_sf + static_cast<size_t>(t) * sf_bytes);
+  if (nsw) {
     uint32_t* sdst = reinterpret_cast<uint32_t*>(xp_sf + static_cast<size_t>(r) * sf_bytes);
-    for (int j = lane; j < (sf_bytes >> 2); j += 32) sdst[j] = __ldg(ssrc + j);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (lane + 32 * u < nsw) sdst[lane + 32 * u] = sv[u];
+    for (int j = lane + 128; j < nsw; j += 32) sdst[j] = __ldg(ssrc + j);
   }
 }
 
