@@ -21,12 +21,13 @@
  *    *_workspace_size() call returns.  Workspaces must be 256-byte aligned.
  *    The exceptions are named where they are declared: the CUDA-graph calls
  *    (moe_forward_graph_create creates a stream and an executable graph,
- *    moe_graph_destroy frees the graph) and the fixed device array of
- *    moe_permute_noalloc.
+ *    moe_graph_destroy frees the graph), the fixed device array of
+ *    moe_permute_noalloc, and the CUDA events that
+ *    moe_forward_host_pipelined creates and destroys within the call.
  *  - Every call is asynchronous on the caller's CUDA stream (`stream` is a
  *    cudaStream_t passed as void*; NULL is the legacy default stream).  The
- *    library does no host synchronisation except in moe_sync_status() and
- *    moe_forward_host().
+ *    library does no host synchronisation except in moe_sync_status(),
+ *    moe_forward_host() and moe_forward_host_pipelined().
  *  - Layouts are row-major with the innermost dimension contiguous.  bf16
  *    tensors are passed as uint16_t bit patterns.
  *  - NVFP4 tensors are three arrays: packed E2M1 codes (uint8, element 2j in
@@ -434,6 +435,27 @@ int moe_forward_host(const moe_layer* L, const uint16_t* x_host, const float* lo
                      int T, uint16_t* out_host,
                      uint16_t* x_dev, float* logits_dev, uint16_t* out_dev,
                      void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward_host over n consecutive batches of T tokens, with the copies
+ * of one batch overlapping the compute of its neighbours (a serving loop:
+ * batch i+1's inputs go to the device and batch i-1's output comes back
+ * while batch i runs).  x_host[i], logits_host[i], out_host[i] (arrays of n
+ * host pointers, bf16 [T,H], fp32 [T,E], bf16 [T,H]) are batch i's buffers,
+ * pinned for asynchronous copies.  x_dev, logits_dev, out_dev are device
+ * buffers of TWO batches each (bf16 [2,T,H], fp32 [2,T,E], bf16 [2,T,H]),
+ * used alternately; ws is one moe_forward workspace for T tokens.  The layer
+ * runs on `stream`, the copies on `copy_stream` (a different, non-NULL
+ * stream; the copies overlap the compute only when neither stream
+ * synchronises with the other, e.g. two streams created non-blocking).  Every out_host[i] holds batch i's result, identical to
+ * moe_forward_host's, when the call returns: both streams are synchronised.
+ * The call creates its CUDA events and destroys them before it returns.
+ * Errors: MOE_ERR_INVALID_ARG for n < 1, a NULL pointer, a NULL
+ * copy_stream, or copy_stream == stream; the moe_forward checks for the
+ * rest. */
+int moe_forward_host_pipelined(const moe_layer* L, int n, const uint16_t* const* x_host,
+                               const float* const* logits_host, int T, uint16_t* const* out_host,
+                               uint16_t* x_dev, float* logits_dev, uint16_t* out_dev,
+                               void* ws, size_t ws_bytes, void* stream, void* copy_stream);
 
 /* moe_forward as a CUDA graph, for launch-bound sizes (decode, small
  * layers): the layer's kernels are captured once on fixed buffers and

@@ -87,6 +87,8 @@ SIGNATURES = {
                                      c_void_p, c_size_t, c_void_p, c_void_p]),
     "moe_forward_host": (c_int, [ctypes.POINTER(MoeLayerC), c_void_p, c_void_p, c_int, c_void_p,
                                  c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_forward_host_pipelined": (c_int, [ctypes.POINTER(MoeLayerC), c_int, c_void_p, c_void_p, c_int, c_void_p,
+                                           c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     "moe_forward_graph_create": (c_int, [ctypes.POINTER(MoeLayerC), c_void_p, c_void_p, c_int, c_void_p,
                                          c_void_p, c_size_t, c_void_p, ctypes.POINTER(c_void_p)]),
     "moe_graph_launch": (c_int, [c_void_p, c_void_p]),

@@ -444,12 +444,49 @@ def moe_forward_host(layer_c, x_host: torch.Tensor, logits_host: torch.Tensor, o
     return out_host
 
 
+def moe_forward_host_pipelined(layer_c, x_host, logits_host, out_host, x_dev: torch.Tensor,
+                               logits_dev: torch.Tensor, out_dev: torch.Tensor, ws: torch.Tensor, stream=None,
+                               copy_stream=None):
+    """n batches of T tokens through moe_forward_host_pipelined: x_host,
+    logits_host, out_host are lists of n pinned host tensors (bf16 [T,H],
+    fp32 [T,E], bf16 [T,H]); x_dev / logits_dev / out_dev hold two batches
+    ([2,T,H], [2,T,E], [2,T,H]).  The layer runs on `stream`, the copies on
+    `copy_stream` (a torch.cuda.Stream other than `stream`)."""
+    import ctypes
+    n = len(x_host)
+    if n < 1 or len(logits_host) != n or len(out_host) != n:
+        raise ValueError("x_host, logits_host, out_host: n >= 1 host tensors each")
+    for nm, t, dt in (("x_dev", x_dev, torch.bfloat16), ("logits_dev", logits_dev, torch.float32),
+                      ("out_dev", out_dev, torch.bfloat16)):
+        _dev(t, nm, dtype=dt)
+        if t.dim() != 3 or t.shape[0] != 2:
+            raise ValueError(f"{nm}: expected two batches [2, T, ...]")
+    T = _forward_args(layer_c, x_dev[0], logits_dev[0], out_dev[0], ws)
+    for i in range(n):
+        _host(x_host[i], f"x_host[{i}]", torch.bfloat16, (T, layer_c.H))
+        _host(logits_host[i], f"logits_host[{i}]", torch.float32, (T, layer_c.E))
+        _host(out_host[i], f"out_host[{i}]", torch.bfloat16, (T, layer_c.H))
+    if copy_stream is None:
+        raise ValueError("copy_stream: required (a stream other than the compute stream)")
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if copy_stream.cuda_stream == stream.cuda_stream:
+        raise ValueError("copy_stream: must differ from the compute stream")
+    ptrs = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+    check(load().moe_forward_host_pipelined(ctypes.byref(layer_c), n, ptrs(x_host), ptrs(logits_host), T,
+                                            ptrs(out_host), _ptr(x_dev), _ptr(logits_dev), _ptr(out_dev),
+                                            _ptr(ws), ws.numel(), stream.cuda_stream, copy_stream.cuda_stream),
+          "moe_forward_host_pipelined")
+    return out_host
+
+
 __all__ = ["MOE_FMT_BF16", "MOE_FMT_NVFP4", "MOE_FMT_MXFP8", "MOE_FMT_MXFP4", "moe_quant_mx", "MOE_EPI_STORE_BF16", "MOE_EPI_SWIGLU_BF16",
            "MOE_EPI_SWIGLU_NVFP4", "moe_version", "moe_sync_status", "moe_set_wait_timeout_ns",
            "moe_selftest_wait_timeout", "moe_selftest_grid_barrier_timeout", "moe_route", "moe_permute",
            "moe_route_permute", "moe_quant_nvfp4", "MOE_EPI_SWIGLU_MX",
            "moe_permute_noalloc", "moe_grouped_gemm", "moe_combine", "moe_shared_gate",
            "moe_forward_workspace_size", "moe_forward", "moe_forward_profiled", "moe_forward_host",
+           "moe_forward_host_pipelined",
            "ForwardGraph"]
 
 

@@ -278,6 +278,70 @@ extern "C" int moe_forward_host(const moe_layer* L, const uint16_t* x_host, cons
   return moe_sync_status(stream);
 }
 
+// Batches alternate between the two halves of the device buffers.  On the
+// copy stream, batch i+1's inputs are enqueued after batch i-1's output copy,
+// which waits for batch i-1's compute: the inputs never overwrite a half
+// still being read.  Batch i's compute waits for its inputs and, from i = 2
+// on, for the copy-out of batch i-2 from the same output half.
+extern "C" int moe_forward_host_pipelined(const moe_layer* L, int n, const uint16_t* const* x_host,
+                                          const float* const* logits_host, int T, uint16_t* const* out_host,
+                                          uint16_t* x_dev, float* logits_dev, uint16_t* out_dev, void* ws,
+                                          size_t ws_bytes, void* stream, void* copy_stream) {
+  MOE_TRY(validate_layer(L));
+  if (n < 1 || T < 0) return MOE_ERR_INVALID_ARG;
+  if (!x_host || !logits_host || !out_host || !x_dev || !logits_dev || !out_dev) return MOE_ERR_INVALID_ARG;
+  if (!copy_stream || stream == copy_stream) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!x_host[i] || !logits_host[i] || !out_host[i]) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream), ps = static_cast<cudaStream_t>(copy_stream);
+  const size_t xe = static_cast<size_t>(T) * L->H, le = static_cast<size_t>(T) * L->E;
+  const size_t xb = xe * sizeof(uint16_t), lb = le * sizeof(float);
+  cudaEvent_t ev[6] = {};  // [0,1] inputs landed, [2,3] compute done, [4,5] output copied, per half
+  int made = 0;
+  cudaError_t e = cudaSuccess;
+  for (; made < 6 && e == cudaSuccess; ++made) e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    --made;  // the failed creation made nothing
+    for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  auto h2d = [&](int i) {
+    const int b = i & 1;
+    cudaError_t r = cudaMemcpyAsync(x_dev + b * xe, x_host[i], xb, cudaMemcpyHostToDevice, ps);
+    if (r == cudaSuccess) r = cudaMemcpyAsync(logits_dev + b * le, logits_host[i], lb, cudaMemcpyHostToDevice, ps);
+    if (r == cudaSuccess) r = cudaEventRecord(ev[b], ps);
+    return r;
+  };
+  int st = MOE_OK;
+  e = h2d(0);
+  for (int i = 0; i < n && e == cudaSuccess && st == MOE_OK; ++i) {
+    const int b = i & 1;
+    e = cudaStreamWaitEvent(cs, ev[b], 0);
+    if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(cs, ev[4 + b], 0);
+    if (e != cudaSuccess) break;
+    st = moe_forward(L, x_dev + b * xe, logits_dev + b * le, T, out_dev + b * xe, ws, ws_bytes, stream);
+    if (st != MOE_OK) break;
+    e = cudaEventRecord(ev[2 + b], cs);
+    if (e == cudaSuccess && i + 1 < n) e = h2d(i + 1);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ps, ev[2 + b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(out_host[i], out_dev + b * xe, xb, cudaMemcpyDeviceToHost, ps);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[4 + b], ps);
+  }
+  // whatever was enqueued finishes before the events go and the call returns
+  cudaError_t e2 = cudaStreamSynchronize(cs);
+  cudaError_t e3 = cudaStreamSynchronize(ps);
+  for (int i = 0; i < 6; ++i) cudaEventDestroy(ev[i]);
+  if (e == cudaSuccess) e = e2 != cudaSuccess ? e2 : e3;
+  if (st != MOE_OK) return st;
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return MOE_ERR_CUDA;
+  }
+  return moe_sync_status(stream);
+}
+
 extern "C" int moe_forward_graph_create(const moe_layer* L, const uint16_t* x, const float* logits, int T,
                                         uint16_t* out, void* ws, size_t ws_bytes, void* stream, void** graph) {
   if (!graph) return MOE_ERR_INVALID_ARG;

@@ -50,6 +50,11 @@ def test_layer_calls_reject_host_tensors():
         m.moe_forward_host(c, x, logits, out, x, logits, out, ws)
     with pytest.raises(ValueError, match="CUDA"):
         m.api.ForwardGraph(c, x, logits, out, ws)  # and its destructor has nothing to free
+    x2, lg2, out2 = x.expand(2, 4, 256).contiguous(), logits.expand(2, 4, 8).contiguous(), out.expand(2, 4, 256).contiguous()
+    with pytest.raises(ValueError, match="CUDA"):
+        m.moe_forward_host_pipelined(c, [x], [logits], [out], x2, lg2, out2, ws)
+    with pytest.raises(ValueError, match="n >= 1"):
+        m.moe_forward_host_pipelined(c, [], [], [], x2, lg2, out2, ws)
     with pytest.raises(ValueError, match="6"):
         m.moe_forward_profiled(c, x, logits, out, ws, [None] * 7)
 

@@ -266,3 +266,30 @@ def test_forward_graph_replays_the_layer(name):
         assert moe_sync_status() == 0
         assert torch.equal(gout, direct)
     graph.close()
+
+
+@pytest.mark.parametrize("name,n", [("tiny", 1), ("tiny", 5), ("deepseek-v3", 4)])
+def test_forward_host_pipelined_equals_each_batch(name, n):
+    """moe_forward_host_pipelined over n batches (copies overlapping the
+    neighbours' compute, device buffers used alternately): every batch's
+    host output equals the direct forward of that batch bit for bit."""
+    from mixture_experts_layer_fwd_gb300 import MoELayer, moe_forward_host_pipelined, moe_sync_status
+    cfg = synth.TINY if name == "tiny" else SMALL[name]
+    T = 64
+    w = synth.make_weights(cfg, seed=5, device=DEV)
+    layer = MoELayer.from_config(cfg, w)
+    acts = [synth.make_activations(cfg, T, seed=10 + i) for i in range(n)]
+    xh = [a.x.pin_memory() for a in acts]
+    lh = [a.logits.pin_memory() for a in acts]
+    oh = [torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    xd = torch.empty(2, T, cfg.H, dtype=torch.bfloat16, device=DEV)
+    ld = torch.empty(2, T, cfg.E, dtype=torch.float32, device=DEV)
+    od = torch.empty(2, T, cfg.H, dtype=torch.bfloat16, device=DEV)
+    ws = layer.workspace(T)
+    compute_stream, copy_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    moe_forward_host_pipelined(layer.c, xh, lh, oh, xd, ld, od, ws, stream=compute_stream, copy_stream=copy_stream)
+    assert moe_sync_status() == 0
+    for i, a in enumerate(acts):
+        direct = layer(a.x.to(DEV), a.logits.to(DEV)).cpu()
+        assert torch.equal(oh[i], direct), i
