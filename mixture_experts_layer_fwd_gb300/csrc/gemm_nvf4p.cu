@@ -51,9 +51,10 @@
 //                 signal
 //   warp 11       in the leader only: the MMA warp's waits (full barrier of
 //                 each stage, accumulator drained at a tile's start)
-//   warps 2..5    epilogue: each CTA reads its 128 accumulator lanes (output
-//                 columns) x tokens, applies the global scales g_a * g_w[e]
-//                 and stores bf16 C[token, col]
+//   warps 2..5,   epilogue, two warps per lane quadrant (even and odd
+//   12..15        32-token chunks): each CTA reads its 128 accumulator lanes
+//                 (output columns) x tokens, applies the global scales
+//                 g_a * g_w[e] and stores bf16 C[token, col]
 // Requires K % 512 == 0 and 16-byte aligned scale arrays.
 #include <cstring>
 
@@ -87,7 +88,8 @@ constexpr int SFB_STRIDE = TN <= 128 ? 4 : 8;     // B columns per MMA (N/32 use
 constexpr int SF_SLOT_COLS = SFB_OFF + SFB_STRIDE * MMAS;
 constexpr int SF_GAP0 = (ACC_STRIDE - TN) / SF_SLOT_COLS;  // slots after the first accumulator
 constexpr int SF_SLOTS = 2;                // scale slots in the gaps after the accumulators
-constexpr int NUM_WARPS = 12;
+constexpr int NUM_WARPS = 16;
+constexpr int W_EPI1 = 12;                 // second set of epilogue warps (12..15)
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int TMEM_COLS = 512;
 constexpr int W_PROD_B = 6, W_SCALE0 = 7, W_WAIT = 11;
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4p_kernel(const __
     for (int b = 0; b < SF_SLOTS; ++b) mbar_init(&sf_empty[b], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);  // 4 epilogue warps of each CTA
+      mbar_init(&tempty[b], 16);  // 8 epilogue warps of each CTA
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4p_kernel(const __
         }
       }
     }
-  } else if (warp >= W_SCALE0) {
+  } else if (warp >= W_SCALE0 && warp < W_SCALE0 + 4) {
     // ===================================================== scale warps (7..10)
     // The 128 threads copy each stage's 32 scale bytes of the CTA's 128
     // weight rows and the tile's token rows (one to three rows each, 16
@@ -453,7 +455,9 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_nvf4p_kernel(const __
       const float scale = __ldg(P.a_g) * __ldg(P.w_g + ti.g);
       const int nch = (ti.cnt + 31) >> 5;
       const int col = ti.blk * 256 + static_cast<int>(rank) * WM + q * 32 + lane;  // output column
-      for (int c = 0; c < nch; ++c) {
+      // two warps per lane quadrant: warps 2..5 take the even 32-token
+      // chunks, warps 12..15 the odd ones
+      for (int c = warp >= W_EPI1 ? 1 : 0; c < nch; c += 2) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + c * 32, v);
         tmem_ld_wait();
