@@ -8,7 +8,9 @@
 //   amax  : grid-stride 16-byte loads, block max, atomicMax of the fp32 bit
 //           pattern (valid ordering for non-negative floats) into workspace
 //   quant : one thread per 16-element block: two 16-byte loads, scale byte,
-//           eight code bytes (one 8-byte store), coalesced across the warp
+//           eight code bytes (one 8-byte store), coalesced across the warp;
+//           for one group (the activations) with the per-group constants
+//           and a per-scale-byte reciprocal table hoisted into shared memory
 #include "internal.h"
 #include "nvfp4.cuh"
 
@@ -72,6 +74,70 @@ __global__ void __launch_bounds__(256) quant_kernel(const uint16_t* __restrict__
   sf[b] = static_cast<uint8_t>(s);
 }
 
+// Pass 2 for one group (the activations): the same codes, scales and g bit
+// for bit, with the per-group work hoisted out of the 16-element blocks.
+// Each thread block computes g, the divisor D = RN(6 g) of the scale step,
+// RN(1 / D), and for every E4M3 scale byte s the decoder's denominator
+// d(s) = RN(e4m3(s) * g) and RN(1 / d(s)) once, in shared memory.  A
+// block's scale is then e4m3(q) with q = RN(amax * RN(1 / D)), which is
+// within 2 ulp of RN(amax / D); the two can round to different E4M3 bytes
+// only near a rounding boundary of E4M3 (a value of at most four
+// significant bits, whose low 19 mantissa bits are zero; above 448 both
+// saturate), so q is replaced by the IEEE quotient when its low 19 mantissa
+// bits lie within 4 of a multiple of 2^19, or when it is not finite.
+__global__ void __launch_bounds__(256) quant1_kernel(const uint16_t* __restrict__ x, long long nblocks,
+                                                     const float* __restrict__ g_in,
+                                                     const unsigned int* __restrict__ amax_bits,
+                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                     float* __restrict__ g_out) {
+  __shared__ float s_den[128], s_rcp[128];
+  __shared__ float s_g;
+  if (threadIdx.x == 0) {
+    float g;
+    if (g_in != nullptr) {
+      g = __ldg(g_in);
+    } else {
+      const float amax = __uint_as_float(__ldg(amax_bits));
+      g = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    }
+    s_g = g;
+    if (blockIdx.x == 0) g_out[0] = g;
+  }
+  __syncthreads();
+  const float g = s_g;
+  if (threadIdx.x < 128) {
+    const float den = __fmul_rn(e4m3_decode(threadIdx.x), g);
+    s_den[threadIdx.x] = den;
+    s_rcp[threadIdx.x] = den != 0.0f ? __frcp_rn(den) : 0.0f;
+  }
+  const float D = __fmul_rn(6.0f, g);
+  const float R = __frcp_rn(D);
+  __syncthreads();
+  const long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (b >= nblocks) return;
+  const uint4* p = reinterpret_cast<const uint4*>(x + b * 16);
+  const uint4 lo = __ldg(p), hi = __ldg(p + 1);
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  float q = __fmul_rn(amax, R);
+  if (((__float_as_uint(q) + 4u) & 0x7FFFFu) <= 8u || !(q < INFINITY)) q = __fdiv_rn(amax, D);
+  const uint32_t sc = e4m3_encode_satfinite(q);  // amax >= 0: a byte in [0, 0x7E]
+  const float den = s_den[sc], r = s_rcp[sc];
+  float qq[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) qq[i] = den != 0.0f ? e2m1_quotient(v[i], den, r) : copysignf(0.0f, v[i]);
+  reinterpret_cast<uint2*>(codes)[b] = make_uint2(e2m1x8_rn_satfinite(qq), e2m1x8_rn_satfinite(qq + 8));
+  sf[b] = static_cast<uint8_t>(sc);
+}
+
 size_t quant_ws_bytes(int groups) { return round_up(static_cast<size_t>(groups) * sizeof(unsigned int), 256); }
 
 int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float* g_in, uint8_t* codes, uint8_t* sf,
@@ -94,8 +160,11 @@ int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float*
   }
   const long long nblocks = group_elems / 16 * groups;
   const long long nthreadblocks = (nblocks + 255) / 256;
-  quant_kernel<<<static_cast<unsigned int>(nthreadblocks), 256, 0, s>>>(x, nblocks, group_elems / 16, g_in, amax,
-                                                                         codes, sf, g_out);
+  if (groups == 1)
+    quant1_kernel<<<static_cast<unsigned int>(nthreadblocks), 256, 0, s>>>(x, nblocks, g_in, amax, codes, sf, g_out);
+  else
+    quant_kernel<<<static_cast<unsigned int>(nthreadblocks), 256, 0, s>>>(x, nblocks, group_elems / 16, g_in, amax,
+                                                                           codes, sf, g_out);
   return check_launch();
 }
 
