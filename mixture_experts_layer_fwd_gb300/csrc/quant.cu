@@ -132,8 +132,18 @@ __global__ void __launch_bounds__(256) quant1_kernel(const uint16_t* __restrict_
   const uint32_t sc = e4m3_encode_satfinite(q);  // amax >= 0: a byte in [0, 0x7E]
   const float den = s_den[sc], r = s_rcp[sc];
   float qq[16];
+  if (den != 0.0f && r < INFINITY) {
+    // |v[i] * r| stays below about 7 for finite inputs: the quotients are
+    // finite, and only the near-decision-point test is left per element
 #pragma unroll
-  for (int i = 0; i < 16; ++i) qq[i] = den != 0.0f ? e2m1_quotient(v[i], den, r) : copysignf(0.0f, v[i]);
+    for (int i = 0; i < 16; ++i) {
+      const float qi = __fmul_rn(v[i], r);
+      qq[i] = ((__float_as_uint(qi) + 8u) & 0x1FFFFFu) <= 16u ? __fdiv_rn(v[i], den) : qi;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qq[i] = den != 0.0f ? e2m1_quotient(v[i], den, r) : copysignf(0.0f, v[i]);
+  }
   reinterpret_cast<uint2*>(codes)[b] = make_uint2(e2m1x8_rn_satfinite(qq), e2m1x8_rn_satfinite(qq + 8));
   sf[b] = static_cast<uint8_t>(sc);
 }
