@@ -9,12 +9,25 @@
 //           pattern (valid ordering for non-negative floats) into workspace
 //   quant : one thread per 16-element block: two 16-byte loads, scale byte,
 //           eight code bytes (one 8-byte store), coalesced across the warp;
-//           for one group (the activations) with the per-group constants
-//           and a per-scale-byte reciprocal table hoisted into shared memory
+//           for one group (the activations) a persistent grid (as many
+//           thread blocks as fit on the SMs at once) whose blocks form the
+//           per-group constants and a per-scale-byte reciprocal table in
+//           shared memory once, then walk the 16-element blocks with the next
+//           block's two loads issued before the current one is encoded
 #include "internal.h"
 #include "nvfp4.cuh"
 
 namespace moe {
+
+// (a * r, b * r), each rounded to nearest even: two fp32 products in one
+// packed instruction
+DEVINL void mul_rn_f32x2(float a, float b, float r, float& ra, float& rb) {
+  unsigned long long x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(r));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(ra), "=f"(rb) : "l"(z));
+}
 
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, long long group_elems,
                                                    unsigned int* __restrict__ amax_bits) {
@@ -74,8 +87,46 @@ __global__ void __launch_bounds__(256) quant_kernel(const uint16_t* __restrict__
   sf[b] = static_cast<uint8_t>(s);
 }
 
+// One 16-element block of quant1_kernel: w holds its 16 bf16 values.
+DEVINL void quant1_block(const uint32_t (&w)[8], long long b, float R, float D, const float* s_den,
+                         const float* s_rcp, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  float q = __fmul_rn(amax, R);
+  if (((__float_as_uint(q) + 4u) & 0x7FFFFu) <= 8u || !(q < INFINITY)) q = __fdiv_rn(amax, D);
+  const uint32_t sc = e4m3_encode_satfinite(q);  // amax >= 0: a byte in [0, 0x7E]
+  const float den = s_den[sc], r = s_rcp[sc];
+  float qq[16];
+  if (den != 0.0f && r < INFINITY) {
+    // only the near-decision-point test is left per element: a product
+    // that overflows is infinite, whose low mantissa bits are zero, so the
+    // test sends it to the division too
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      float q0, q1;
+      mul_rn_f32x2(v[i], v[i + 1], r, q0, q1);
+      qq[i] = ((__float_as_uint(q0) + 8u) & 0x1FFFFFu) <= 16u ? __fdiv_rn(v[i], den) : q0;
+      qq[i + 1] = ((__float_as_uint(q1) + 8u) & 0x1FFFFFu) <= 16u ? __fdiv_rn(v[i + 1], den) : q1;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qq[i] = den != 0.0f ? e2m1_quotient(v[i], den, r) : copysignf(0.0f, v[i]);
+  }
+  reinterpret_cast<uint2*>(codes)[b] = make_uint2(e2m1x8_rn_satfinite(qq), e2m1x8_rn_satfinite(qq + 8));
+  sf[b] = static_cast<uint8_t>(sc);
+}
+
 // Pass 2 for one group (the activations): the same codes, scales and g bit
-// for bit, with the per-group work hoisted out of the 16-element blocks.
+// for bit, with the per-group work hoisted out of the 16-element blocks
+// (once per thread block of a persistent grid: thread t of block c encodes
+// 16-element blocks t + 256 c, t + 256 (c + grid), ...).
 // Each thread block computes g, the divisor D = RN(6 g) of the scale step,
 // RN(1 / D), and for every E4M3 scale byte s the decoder's denominator
 // d(s) = RN(e4m3(s) * g) and RN(1 / d(s)) once, in shared memory.  A
@@ -113,39 +164,22 @@ __global__ void __launch_bounds__(256) quant1_kernel(const uint16_t* __restrict_
   const float D = __fmul_rn(6.0f, g);
   const float R = __frcp_rn(D);
   __syncthreads();
-  const long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   if (b >= nblocks) return;
-  const uint4* p = reinterpret_cast<const uint4*>(x + b * 16);
-  const uint4 lo = __ldg(p), hi = __ldg(p + 1);
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  float v[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    v[2 * j] = __uint_as_float(w[j] << 16);
-    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-  }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  float q = __fmul_rn(amax, R);
-  if (((__float_as_uint(q) + 4u) & 0x7FFFFu) <= 8u || !(q < INFINITY)) q = __fdiv_rn(amax, D);
-  const uint32_t sc = e4m3_encode_satfinite(q);  // amax >= 0: a byte in [0, 0x7E]
-  const float den = s_den[sc], r = s_rcp[sc];
-  float qq[16];
-  if (den != 0.0f && r < INFINITY) {
-    // |v[i] * r| stays below about 7 for finite inputs: the quotients are
-    // finite, and only the near-decision-point test is left per element
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float qi = __fmul_rn(v[i], r);
-      qq[i] = ((__float_as_uint(qi) + 8u) & 0x1FFFFFu) <= 16u ? __fdiv_rn(v[i], den) : qi;
+  const uint4* p = reinterpret_cast<const uint4*>(x);
+  uint4 lo = __ldg(p + 2 * b), hi = __ldg(p + 2 * b + 1);
+  for (; b < nblocks; b += stride) {
+    uint4 next_lo = make_uint4(0u, 0u, 0u, 0u), next_hi = next_lo;
+    if (b + stride < nblocks) {
+      next_lo = __ldg(p + 2 * (b + stride));
+      next_hi = __ldg(p + 2 * (b + stride) + 1);
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) qq[i] = den != 0.0f ? e2m1_quotient(v[i], den, r) : copysignf(0.0f, v[i]);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    lo = next_lo;
+    hi = next_hi;
+    quant1_block(w, b, R, D, s_den, s_rcp, codes, sf);
   }
-  reinterpret_cast<uint2*>(codes)[b] = make_uint2(e2m1x8_rn_satfinite(qq), e2m1x8_rn_satfinite(qq + 8));
-  sf[b] = static_cast<uint8_t>(sc);
 }
 
 size_t quant_ws_bytes(int groups) { return round_up(static_cast<size_t>(groups) * sizeof(unsigned int), 256); }
@@ -170,8 +204,17 @@ int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float*
   }
   const long long nblocks = group_elems / 16 * groups;
   const long long nthreadblocks = (nblocks + 255) / 256;
-  if (groups == 1)
-    quant1_kernel<<<static_cast<unsigned int>(nthreadblocks), 256, 0, s>>>(x, nblocks, g_in, amax, codes, sf, g_out);
+  if (groups == 1) {
+    // as many thread blocks as are resident at once
+    static int per_sm = 0;
+    if (per_sm == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant1_kernel, 256, 0) != cudaSuccess || n < 1) n = 1;
+      per_sm = n;
+    }
+    const long long grid = std::min<long long>(nthreadblocks, static_cast<long long>(per_sm) * num_sms());
+    quant1_kernel<<<static_cast<unsigned int>(grid), 256, 0, s>>>(x, nblocks, g_in, amax, codes, sf, g_out);
+  }
   else
     quant_kernel<<<static_cast<unsigned int>(nthreadblocks), 256, 0, s>>>(x, nblocks, group_elems / 16, g_in, amax,
                                                                            codes, sf, g_out);
