@@ -33,6 +33,7 @@
 // is resident and every arrival comes.  Each wait is bounded in wall time
 // (moe_set_wait_timeout_ns): a wait that runs out records MOE_ERR_TIMEOUT in
 // the device error word and the block returns.
+#include <atomic>
 #include <cstring>
 
 #include "internal.h"
@@ -323,8 +324,11 @@ template <int EPL, bool TO_F16>
 int launch_epl(const DispatchArgs& a, int grid, cudaStream_t s) {
   // E counters + kWarps x E per-warp counts (up to 132 KB at E = 1024)
   const size_t smem = static_cast<size_t>(a.E) * (1 + kWarps) * sizeof(int32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the attribute is per device; a racing first call sets the same value
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev].load(std::memory_order_relaxed)) {
     const int max_dyn = static_cast<int>(static_cast<size_t>(kMaxE) * (1 + kWarps) * sizeof(int32_t));
     cudaError_t e = cudaFuncSetAttribute(route_permute_kernel<EPL, TO_F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
@@ -332,7 +336,7 @@ int launch_epl(const DispatchArgs& a, int grid, cudaStream_t s) {
       set_cuda_error(e);
       return MOE_ERR_CUDA;
     }
-    attr_set = true;
+    attr_set[dev].store(true, std::memory_order_relaxed);
   }
   return launch_cooperative(route_permute_kernel<EPL, TO_F16>, grid, smem, s, a);
 }

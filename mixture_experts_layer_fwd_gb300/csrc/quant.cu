@@ -14,6 +14,8 @@
 //           per-group constants and a per-scale-byte reciprocal table in
 //           shared memory once, then walk the 16-element blocks with the next
 //           block's two loads issued before the current one is encoded
+#include <atomic>
+
 #include "internal.h"
 #include "nvfp4.cuh"
 
@@ -205,12 +207,16 @@ int quant_launch(const uint16_t* x, int groups, int rows, int cols, const float*
   const long long nblocks = group_elems / 16 * groups;
   const long long nthreadblocks = (nblocks + 255) / 256;
   if (groups == 1) {
-    // as many thread blocks as are resident at once
-    static int per_sm = 0;
+    // as many thread blocks as are resident at once (per device; a racing
+    // first call stores the same value)
+    static std::atomic<int> resident[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int per_sm = resident[dev].load(std::memory_order_relaxed);
     if (per_sm == 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant1_kernel, 256, 0) != cudaSuccess || n < 1) n = 1;
-      per_sm = n;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant1_kernel, 256, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+      resident[dev].store(per_sm, std::memory_order_relaxed);
     }
     const long long grid = std::min<long long>(nthreadblocks, static_cast<long long>(per_sm) * num_sms());
     quant1_kernel<<<static_cast<unsigned int>(grid), 256, 0, s>>>(x, nblocks, g_in, amax, codes, sf, g_out);

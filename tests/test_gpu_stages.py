@@ -183,9 +183,13 @@ def test_route_permute_matches_oracle_and_split_calls(name, T):
 
 def test_route_permute_nvfp4_rows_scales_and_variants():
     """Packed rows with scale bytes, the router without renormalisation, hot
-    experts that leave others empty, E = 1024 (the router's limit)."""
+    experts that leave others empty, E = 1024 (the router's limit) with few
+    and with many slots per block (placement by one warp, and split over a
+    block's warps), and blocks of more than 4096 slots (k = 32: placement in
+    several staged pieces)."""
     m = api()
-    for T, E, k, renorm in ((3000, 64, 4, True), (700, 1024, 8, False), (5, 16, 16, True)):
+    for T, E, k, renorm in ((3000, 64, 4, True), (700, 1024, 8, False), (5, 16, 16, True), (8192, 1024, 8, True),
+                            (20000, 64, 32, True)):
         g = torch.Generator().manual_seed(T)
         rank = torch.randperm(E, generator=g).double() + 1
         logits = (torch.randn(T, E, generator=g, dtype=torch.float64) - 2.0 * torch.log(rank)).float()
@@ -201,8 +205,26 @@ def test_route_permute_nvfp4_rows_scales_and_variants():
         assert np.array_equal(r["row_of"].cpu().numpy(), p.row_of)
         src = torch.from_numpy(p.src_tok).long()
         assert torch.equal(r["xp"].cpu(), rows[src]) and torch.equal(r["xp_sf"].cpu(), sf[src])
-        if E == 64:
+        if (T, E) == (3000, 64):  # hot experts leave others empty
             assert (p.counts == 0).any()
+
+
+def test_route_permute_ties_and_signed_zero():
+    """Exact ties (lower expert id first) and -0.0 next to +0.0 through the
+    fused dispatch, with enough tokens per block to split the placement."""
+    m = api()
+    g = torch.Generator().manual_seed(3)
+    logits = torch.round(torch.randn(40000, 64, generator=g) * 2) / 2  # many exact ties
+    logits[0] = 0.0
+    logits[1, ::2] = -0.0
+    r = m.moe_route_permute(logits.to(DEV), 8)
+    _sync()
+    ridx, rw = oracle.route(logits.numpy(), 8)
+    assert np.array_equal(r["idx"].cpu().numpy(), ridx)
+    np.testing.assert_allclose(r["w"].cpu().numpy().astype(np.float64), rw, rtol=1e-6, atol=0)
+    p = oracle.permute(ridx, 64)
+    for key, ref in (("counts", p.counts), ("offsets", p.offsets), ("row_of", p.row_of), ("src_tok", p.src_tok)):
+        assert np.array_equal(r[key].cpu().numpy(), ref), key
 
 
 # ----------------------------------------------------------------- quant ----
