@@ -63,13 +63,14 @@ class MoELayer:
                  w_fmt: str = "bf16", act_fmt: str = "bf16", g_h: float = 0.0, g_hs: Optional[float] = None,
                  renorm: bool = True, shared_gate: Optional[torch.Tensor] = None):
         """w13 bf16 [E, 2I, H], w2 bf16 [E, H, I], ws13 bf16 [2I_s, H], ws2 bf16
-        [H, I_s] on one CUDA device.  With w_fmt='nvfp4' they are quantised
+        [H, I_s] on one CUDA device.  With w_fmt='nvfp4' (or 'mxfp8' /
+        'mxfp4', whose act_fmt must be the same format) they are quantised
         here; act_fmt='nvfp4' also needs the static global scale g_h of the
         SwiGLU output (g_hs for the shared expert, default g_h).
         renorm=False routes without renormalisation; shared_gate (bf16 [H])
         scales the shared expert by sigmoid(x . shared_gate)."""
         if w_fmt not in _FMT or act_fmt not in _FMT:
-            raise ValueError(f"formats: expected 'bf16' or 'nvfp4', got {w_fmt!r}, {act_fmt!r}")
+            raise ValueError(f"formats: expected one of {sorted(_FMT)}, got {w_fmt!r}, {act_fmt!r}")
         _check_weight(w13, "w13", (E, 2 * I, H))
         _check_weight(w2, "w2", (E, H, I), w13.device)
         if I_s:
